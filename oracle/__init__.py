@@ -1,0 +1,176 @@
+"""Oracle for k-quant decoding and products: ctypes wrapper around kq_oracle.c.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package; the product library never
+does, and the two share no code.  ``build()`` compiles the C source with gcc
+(fp64 loops, OpenMP over output rows).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "kq_oracle.c")
+LIB = os.path.join(HERE, "libkq_oracle.so")
+
+Q4_K, Q5_K, Q6_K = 1, 2, 3
+X_F32, X_BF16 = 0, 1
+BLOCK_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into libkq_oracle.so next to its source."""
+    hdr = os.path.join(HERE, "kq_oracle.h")
+    if (not force and os.path.exists(LIB)
+            and os.path.getmtime(LIB) >= max(os.path.getmtime(SRC), os.path.getmtime(hdr))):
+        return LIB
+    tmp = LIB + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp",
+                           "-o", tmp, SRC, "-lm"])
+    os.replace(tmp, LIB)
+    return LIB
+
+
+class _Fields(ctypes.Structure):
+    _fields_ = [("d_bits", ctypes.c_uint16), ("dmin_bits", ctypes.c_uint16),
+                ("sc", ctypes.c_int * 16), ("m", ctypes.c_int * 8), ("q", ctypes.c_int * 256)]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = bind(LIB)
+    return _lib
+
+
+def use_library(path: str | None):
+    """Point this wrapper at another build of the oracle source (the pin tests
+    use this to check that deliberately broken copies fail); None restores."""
+    global _lib
+    _lib = bind(path) if path else None
+
+
+def bind(path: str):
+    """Load one build of the oracle and declare its C signatures."""
+    L = ctypes.CDLL(path)
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.oracle_block_bytes.argtypes = [I]
+    L.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+    L.oracle_half_to_double.restype = ctypes.c_double
+    L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    L.oracle_bf16_to_double.restype = ctypes.c_double
+    L.oracle_unpack.argtypes = [I, P, ctypes.POINTER(_Fields)]
+    L.oracle_pack.argtypes = [I, ctypes.POINTER(_Fields), P]
+    L.oracle_dequant_block_f64.argtypes = [I, P, P]
+    L.oracle_dequant.argtypes = [I, P, I64, P]
+    L.oracle_matvec.argtypes = [I, P, I64, I64, P, I, I64, P, P, I]
+    L.oracle_moe_matvec.argtypes = [I, P, I, P, P, P, I, I, I64, I64, I64, I, P, P, I]
+    return L
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def half_to_double(bits: int) -> float:
+    return lib().oracle_half_to_double(int(bits))
+
+
+def bf16_to_double(bits: int) -> float:
+    return lib().oracle_bf16_to_double(int(bits))
+
+
+def unpack(qtype: int, blk: np.ndarray) -> dict:
+    """Integer fields of one block: d_bits, dmin_bits, sc, m, q (unbiased codes)."""
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    assert blk.size == BLOCK_BYTES[qtype]
+    f = _Fields()
+    rc = lib().oracle_unpack(qtype, _ptr(blk), ctypes.byref(f))
+    assert rc == 0
+    nsc = 16 if qtype == Q6_K else 8
+    return {"d_bits": f.d_bits, "dmin_bits": f.dmin_bits,
+            "sc": np.array(f.sc[:nsc], dtype=np.int32), "m": np.array(f.m[:8], dtype=np.int32),
+            "q": np.array(f.q[:], dtype=np.int32)}
+
+
+def pack(qtype: int, d_bits: int, sc, q, dmin_bits: int = 0, m=None) -> np.ndarray:
+    """Build one block's bytes from integer fields."""
+    f = _Fields()
+    f.d_bits, f.dmin_bits = int(d_bits), int(dmin_bits)
+    for i, v in enumerate(sc):
+        f.sc[i] = int(v)
+    if m is not None:
+        for i, v in enumerate(m):
+            f.m[i] = int(v)
+    for i, v in enumerate(q):
+        f.q[i] = int(v)
+    out = np.zeros(BLOCK_BYTES[qtype], dtype=np.uint8)
+    assert lib().oracle_pack(qtype, ctypes.byref(f), _ptr(out)) == 0
+    return out
+
+
+def dequant_block_f64(qtype: int, blk: np.ndarray) -> np.ndarray:
+    blk = np.ascontiguousarray(blk, dtype=np.uint8)
+    w = np.zeros(256, dtype=np.float64)
+    assert lib().oracle_dequant_block_f64(qtype, _ptr(blk), _ptr(w)) == 0
+    return w
+
+
+def dequant(qtype: int, blocks: np.ndarray) -> np.ndarray:
+    """All blocks (any shape ending in a multiple of the block size) -> fp32 weights."""
+    raw = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1)
+    nb = raw.size // BLOCK_BYTES[qtype]
+    assert nb * BLOCK_BYTES[qtype] == raw.size
+    out = np.zeros(nb * 256, dtype=np.float32)
+    assert lib().oracle_dequant(qtype, _ptr(raw), nb, _ptr(out)) == 0
+    return out
+
+
+def _x_arg(x: np.ndarray):
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, X_F32
+    if x.dtype == np.uint16:  # bfloat16 bit patterns
+        return x, X_BF16
+    raise TypeError("x must be float32 or uint16 (bfloat16 bits)")
+
+
+def matvec(qtype: int, W: np.ndarray, N: int, K: int, x: np.ndarray, threads: int = 1):
+    """Returns (y, s), both float64 of shape (M, N); x has shape (M, K)."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    x, xd = _x_arg(x)
+    M = x.size // K if K else (x.shape[0] if x.ndim == 2 else 0)
+    y = np.zeros((M, N), dtype=np.float64)
+    s = np.zeros((M, N), dtype=np.float64)
+    rc = lib().oracle_matvec(qtype, _ptr(W), N, K, _ptr(x), xd, M, _ptr(y), _ptr(s), threads)
+    assert rc == 0, rc
+    return y, s
+
+
+def moe_matvec(qtype: int, W_experts: np.ndarray, n_experts: int, ids: np.ndarray,
+               gate, x: np.ndarray, x_per_slot: bool, N: int, K: int, M: int, top_k: int,
+               threads: int = 1):
+    """Routed-expert product; returns (y, s) float64 ([M,top_k,N] without gate, [M,N] with)."""
+    W_experts = np.ascontiguousarray(W_experts, dtype=np.uint8)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    x, xd = _x_arg(x)
+    shape = (M, N) if gate is not None else (M, top_k, N)
+    y = np.zeros(shape, dtype=np.float64)
+    s = np.zeros(shape, dtype=np.float64)
+    g = None
+    if gate is not None:
+        g = np.ascontiguousarray(gate, dtype=np.float32)
+    rc = lib().oracle_moe_matvec(qtype, _ptr(W_experts), n_experts, _ptr(ids),
+                                 _ptr(g) if g is not None else None, _ptr(x), xd,
+                                 int(bool(x_per_slot)), N, K, M, top_k, _ptr(y), _ptr(s), threads)
+    if rc != 0:
+        raise ValueError(f"oracle_moe_matvec failed: {rc}")
+    return y, s

@@ -1,0 +1,302 @@
+"""Pins for the oracle: each checks it against something other than itself.
+
+* IEEE-754 decoders against numpy's float16 and torch's bfloat16 (all patterns);
+* the integer field decoder against an independent bit-position reader;
+* pack <-> unpack round trips in both directions (the layouts are bijections);
+* hand-built blocks with closed-form weights (tests/golden/handbuilt_blocks.txt);
+* closed forms: constant fields, one-hot scales and mins, the Q6_K zero point;
+* the product against plain integer / float matrix products (numpy matmul) on
+  tiny matrices, linearity in x, zero x, weights past K ignored;
+* the routed-expert product against per-slot products and brute force.
+
+All run on the CPU.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import tests.bitref as bitref
+from gguf_quant_weight_super_gb300 import synth
+
+Q4_K, Q5_K, Q6_K = 1, 2, 3
+TYPES = [Q4_K, Q5_K, Q6_K]
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "handbuilt_blocks.txt")
+
+
+def test_block_sizes(orc):
+    lib = orc.lib()
+    assert [lib.oracle_block_bytes(t) for t in TYPES] == [144, 176, 210]
+    assert lib.oracle_block_bytes(0) == 0 and lib.oracle_block_bytes(4) == 0
+    # bits per weight: 4.5, 5.5, 6.5625
+    assert [lib.oracle_block_bytes(t) * 8 / 256 for t in TYPES] == [4.5, 5.5, 6.5625]
+
+
+def test_half_decoder_all_patterns(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([orc.half_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_bf16_decoder_all_patterns(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([orc.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+def test_unpack_matches_bit_reader(orc, qtype):
+    g = synth.rng(100, qtype)
+    blocks = g.integers(0, 256, size=(3000, synth.BLOCK_BYTES[qtype]), dtype=np.uint8)
+    if qtype == Q6_K:
+        d, sc, q = bitref.q6k(blocks)
+    else:
+        d, dmin, sc, m, q = bitref.q4k_like(blocks, five_bit=(qtype == Q5_K))
+    for i in range(len(blocks)):
+        f = orc.unpack(qtype, blocks[i])
+        assert f["d_bits"] == d[i]
+        assert np.array_equal(f["sc"], sc[i])
+        assert np.array_equal(f["q"], q[i])
+        if qtype != Q6_K:
+            assert f["dmin_bits"] == dmin[i]
+            assert np.array_equal(f["m"], m[i])
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+def test_bytes_unpack_pack_roundtrip(orc, qtype):
+    g = synth.rng(101, qtype)
+    blocks = g.integers(0, 256, size=(500, synth.BLOCK_BYTES[qtype]), dtype=np.uint8)
+    for blk in blocks:
+        f = orc.unpack(qtype, blk)
+        again = orc.pack(qtype, f["d_bits"], f["sc"], f["q"], f["dmin_bits"], f["m"])
+        assert np.array_equal(again, blk)
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+def test_fields_pack_unpack_roundtrip(orc, qtype):
+    g = synth.rng(102, qtype)
+    qmax = {Q4_K: 15, Q5_K: 31, Q6_K: 63}[qtype]
+    for _ in range(300):
+        q = g.integers(0, qmax + 1, 256)
+        if qtype == Q6_K:
+            sc = g.integers(-128, 128, 16)
+            m = None
+        else:
+            sc = g.integers(0, 64, 8)
+            m = g.integers(0, 64, 8)
+        d, dm = (int(v) for v in g.integers(0, 65536, 2))
+        blk = orc.pack(qtype, d, sc, q, dm, m)
+        f = orc.unpack(qtype, blk)
+        assert f["d_bits"] == d and np.array_equal(f["q"], q) and np.array_equal(f["sc"], sc)
+        if m is not None:
+            assert f["dmin_bits"] == dm and np.array_equal(f["m"], m)
+
+
+def _golden_cases():
+    cases = []
+    with open(GOLDEN) as fh:
+        lines = [ln.rstrip("\n") for ln in fh if not ln.startswith("#")]
+    for i in range(0, len(lines), 3):
+        name = lines[i].split()[1]
+        blk = np.frombuffer(bytes.fromhex(lines[i + 1].split()[1]), dtype=np.uint8)
+        w = np.array([float(v) for v in lines[i + 2].split()[1:]])
+        cases.append(({"Q4_K": Q4_K, "Q5_K": Q5_K, "Q6_K": Q6_K}[name], blk, w, lines[i]))
+    return cases
+
+
+def test_golden_handbuilt_blocks(orc):
+    cases = _golden_cases()
+    assert len(cases) >= 5
+    for qtype, blk, w, desc in cases:
+        got = orc.dequant_block_f64(qtype, blk)
+        assert np.array_equal(got, w), desc
+        assert np.array_equal(orc.dequant(qtype, blk), w.astype(np.float32)), desc
+        assert np.array_equal(bitref.dequant_f64(qtype, blk[None])[0], w), desc
+
+
+@pytest.mark.parametrize("qtype", [Q4_K, Q5_K])
+def test_closed_form_constant_fields(orc, qtype):
+    g = synth.rng(103, qtype)
+    qmax = 15 if qtype == Q4_K else 31
+    for _ in range(50):
+        q0, s, t = int(g.integers(0, qmax + 1)), int(g.integers(0, 64)), int(g.integers(0, 64))
+        dh, mh = np.abs(g.normal(0, 0.01, 2)).astype(np.float16)
+        blk = orc.pack(qtype, int(dh.view(np.uint16)), [s] * 8, [q0] * 256, int(mh.view(np.uint16)), [t] * 8)
+        expect = float(dh) * s * q0 - float(mh) * t
+        assert np.all(orc.dequant_block_f64(qtype, blk) == expect)
+
+
+@pytest.mark.parametrize("qtype", [Q4_K, Q5_K])
+def test_one_hot_scale_and_min(orc, qtype):
+    g = synth.rng(104, qtype)
+    qmax = 15 if qtype == Q4_K else 31
+    q = g.integers(0, qmax + 1, 256)
+    for j in range(8):
+        sc = [0] * 8
+        sc[j] = 1
+        blk = orc.pack(qtype, 0x3C00, sc, q, 0x3C00, [0] * 8)
+        w = orc.dequant_block_f64(qtype, blk)
+        inside = np.zeros(256, bool)
+        inside[32 * j:32 * j + 32] = True
+        assert np.array_equal(w[inside], q[inside].astype(np.float64))
+        assert np.all(w[~inside] == 0)
+        m = [0] * 8
+        m[j] = 1
+        blk = orc.pack(qtype, 0x3C00, [0] * 8, q, 0x3C00, m)
+        w = orc.dequant_block_f64(qtype, blk)
+        assert np.all(w[inside] == -1.0) and np.all(w[~inside] == 0)
+
+
+def test_q6k_zero_point_and_one_hot(orc):
+    g = synth.rng(105)
+    sc = g.integers(-128, 128, 16)
+    blk = orc.pack(Q6_K, 0x3C00, sc, [32] * 256)
+    assert np.all(orc.dequant_block_f64(Q6_K, blk) == 0)
+    q = g.integers(0, 64, 256)
+    for j in range(16):
+        s = [0] * 16
+        s[j] = 1
+        w = orc.dequant_block_f64(Q6_K, orc.pack(Q6_K, 0x3C00, s, q))
+        inside = np.zeros(256, bool)
+        inside[16 * j:16 * j + 16] = True
+        assert np.array_equal(w[inside], (q[inside] - 32).astype(np.float64))
+        assert np.all(w[~inside] == 0)
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+def test_dequant_matches_bit_reader_and_rounds_once(orc, qtype):
+    g = synth.rng(106, qtype)
+    blocks = synth.gen_blocks(qtype, 400, g)
+    ref = bitref.dequant_f64(qtype, blocks)
+    w64 = np.stack([orc.dequant_block_f64(qtype, b) for b in blocks])
+    assert np.array_equal(w64, ref)
+    assert np.array_equal(orc.dequant(qtype, blocks).reshape(-1, 256), ref.astype(np.float32))
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("x_dtype", ["f32", "bf16"])
+def test_matvec_integer_special_case(orc, qtype, x_dtype):
+    """d = 1, sc = 1, m = 0: weights are the integer codes (minus 32 for Q6_K), so
+    the product is a plain integer-matrix times vector (numpy matmul)."""
+    g = synth.rng(107, qtype)
+    N, K = 5, 512
+    qmax = {Q4_K: 15, Q5_K: 31, Q6_K: 63}[qtype]
+    codes = g.integers(0, qmax + 1, (N, K))
+    blocks = []
+    for n in range(N):
+        for b in range(K // 256):
+            q = codes[n, 256 * b:256 * b + 256]
+            if qtype == Q6_K:
+                blocks.append(orc.pack(qtype, 0x3C00, [1] * 16, q))
+            else:
+                blocks.append(orc.pack(qtype, 0x3C00, [1] * 8, q, 0x3C00, [0] * 8))
+    W = np.concatenate(blocks)
+    x = synth.gen_x(3, K, g, x_dtype)
+    xf = x.astype(np.float64) if x_dtype == "f32" else \
+        torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double().numpy()
+    wint = (codes - 32) if qtype == Q6_K else codes
+    y, s = orc.matvec(qtype, W, N, K, x)
+    ref = xf @ wint.T.astype(np.float64)
+    assert np.allclose(y, ref, rtol=1e-13, atol=1e-12)
+    assert np.allclose(s, np.abs(xf) @ np.abs(wint).T, rtol=1e-13)
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("NK", [(1, 256), (3, 512), (4, 768)])
+def test_matvec_brute_force(orc, qtype, NK):
+    N, K = NK
+    g = synth.rng(108, qtype, N, K)
+    W = synth.gen_matrix(qtype, N, K, g)
+    x = synth.gen_x(2, K, g, "f32")
+    wd = bitref.dequant_f64(qtype, W.reshape(-1, synth.BLOCK_BYTES[qtype])).reshape(N, -1)[:, :K]
+    y, s = orc.matvec(qtype, W, N, K, x)
+    ref = x.astype(np.float64) @ wd.T
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-15)
+    assert np.allclose(s, np.abs(x.astype(np.float64)) @ np.abs(wd).T, rtol=1e-12)
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+def test_matvec_linearity_and_zero(orc, qtype):
+    N, K = 6, 768
+    g = synth.rng(109, qtype)
+    W = synth.gen_matrix(qtype, N, K, g)
+    x1 = synth.gen_x(1, K, g)
+    x2 = synth.gen_x(1, K, g)
+    y1, _ = orc.matvec(qtype, W, N, K, x1)
+    y2, _ = orc.matvec(qtype, W, N, K, x2)
+    # power-of-two coefficients keep a*x1 + b*x2 nearly exact in fp32
+    x3 = (np.float32(2.0) * x1 - np.float32(0.5) * x2).astype(np.float32)
+    y3, _ = orc.matvec(qtype, W, N, K, x3)
+    assert np.allclose(y3, 2.0 * y1 - 0.5 * y2, rtol=1e-6, atol=1e-9)
+    y0, s0 = orc.matvec(qtype, W, N, K, np.zeros((1, K), np.float32))
+    assert np.all(y0 == 0) and np.all(s0 == 0)
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+def test_matvec_weights_past_K_ignored(orc, qtype):
+    N, K = 3, 704          # 3 blocks per row, the last one covers 192 weights
+    g = synth.rng(110, qtype)
+    W = synth.gen_matrix(qtype, N, K, g)
+    x = synth.gen_x(2, K, g)
+    y, _ = orc.matvec(qtype, W, N, K, x)
+    wd = bitref.dequant_f64(qtype, W.reshape(-1, synth.BLOCK_BYTES[qtype])).reshape(N, -1)[:, :K]
+    assert np.allclose(y, x.astype(np.float64) @ wd.T, rtol=1e-12, atol=1e-15)
+    # rewriting the codes of the part of each row past K changes nothing
+    nbytes = synth.BLOCK_BYTES[qtype]
+    W2 = W.copy().reshape(N, 3, nbytes)
+    if qtype == Q4_K:
+        W2[:, 2, 16 + 96:16 + 128] ^= 0xFF      # chunk 3 = weights 192..255
+    elif qtype == Q6_K:
+        W2[:, 2, 64 + 0:64 + 64] ^= 0xF0        # high nibbles of half 1 = weights 192..255
+    y2, _ = orc.matvec(qtype, W2.reshape(-1), N, K, x)
+    assert np.array_equal(y, y2)
+
+
+@pytest.mark.parametrize("with_gate", [False, True])
+@pytest.mark.parametrize("x_per_slot", [False, True])
+def test_moe_matches_per_slot_products(orc, with_gate, x_per_slot):
+    qtype, E, N, K, M, top_k = Q4_K, 6, 5, 512, 3, 2
+    g = synth.rng(111, int(with_gate), int(x_per_slot))
+    We = synth.gen_matrix(qtype, E * N, K, g)
+    ids, gate = synth.gen_routing(M, E, top_k, g)
+    x = synth.gen_x(M * top_k if x_per_slot else M, K, g, "bf16")
+    y, s = orc.moe_matvec(qtype, We, E, ids, gate if with_gate else None, x, x_per_slot, N, K, M, top_k)
+    eb = N * 2 * 144
+    per = np.zeros((M, top_k, N))
+    per_abs = np.zeros((M, top_k, N))
+    for m in range(M):
+        for t in range(top_k):
+            e = ids[m, t]
+            xr = x[m * top_k + t] if x_per_slot else x[m]
+            yy, ss = orc.matvec(qtype, We[e * eb:(e + 1) * eb], N, K, xr[None])
+            per[m, t], per_abs[m, t] = yy[0], ss[0]
+    if with_gate:
+        ref = (gate.astype(np.float64)[:, :, None] * per).sum(axis=1)
+        ref_abs = (np.abs(gate.astype(np.float64))[:, :, None] * per_abs).sum(axis=1)
+        assert np.allclose(y, ref, rtol=1e-13, atol=1e-15) and np.allclose(s, ref_abs, rtol=1e-13)
+    else:
+        assert np.array_equal(y, per) and np.array_equal(s, per_abs)
+
+
+def test_moe_rejects_bad_expert_id(orc):
+    g = synth.rng(112)
+    We = synth.gen_matrix(Q4_K, 2 * 4, 256, g)
+    x = synth.gen_x(1, 256, g)
+    with pytest.raises(ValueError):
+        orc.moe_matvec(Q4_K, We, 2, np.array([[0, 2]], np.int32), None, x, False, 4, 256, 1, 2)
+
+
+def test_routing_generator_is_top_k_softmax():
+    g = synth.rng(113)
+    ids, gate = synth.gen_routing(16, 128, 8, g)
+    assert ids.shape == (16, 8) and gate.shape == (16, 8)
+    assert all(len(set(r)) == 8 for r in ids)
+    assert np.allclose(gate.sum(axis=1), 1.0, atol=1e-6) and np.all(np.diff(gate, axis=1) <= 0)
