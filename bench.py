@@ -1,0 +1,344 @@
+"""Benchmark: decode-step products against a 4B-class Q4_K_M decoder on GB300.
+
+One step = one token through the whole weight stream of a 36-layer dense
+decoder (hidden 2560; q 2560->4096, k/v 2560->1024, o 4096->2560, gate/up
+2560->9728, down 9728->2560; LM head 2560->151936), Q4_K everywhere except
+Q6_K for v_proj and down_proj on even layers and for the LM head.  Every
+matrix is a separate kq_matvec call in decode order (q, k, v share an input;
+gate, up share an input); the whole step is captured in a CUDA graph whose
+kernels are chained with programmatic dependent launch.
+
+Prints one JSON line.  `value` is quantized-weight GB/s (stored weight bytes
+read per second); tok/s-equivalent = steps per second.  Inputs are synthetic
+(seeded), weights resident in HBM before timing; the weight set (2.49 GB) is
+far larger than L2, so no flushing is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kq|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+import zlib
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized-weight GB/s and equiv. decode tok/s vs 8 TB/s HBM roofline"
+WORKLOAD = "4B-class dense decoder, 36 layers + LM head, Q4_K_M mix (Q6_K v/down on even layers and head), M=1, bf16 x"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def build_model(torch, synth, seed=0):
+    """Weights and per-stage inputs/outputs for one token of the sweep."""
+    stages = synth.dense_layer_sweep()
+    dev = torch.device("cuda")
+    mats, xs = [], []
+    for si, st in enumerate(stages):
+        K = st[0][3]
+        g = synth.rng(seed, 1000 + si)
+        xs.append(torch.from_numpy(synth.gen_x(1, K, g, "bf16").view(np.int16)).to(dev).view(torch.bfloat16))
+        for (name, qt, N, K_) in st:
+            gm = synth.rng(seed, 1000 + si, zlib.crc32(name.encode()) & 0xFFFF)
+            kw = {"q6_scale_range": (-32, 31)} if qt == synth.Q6_K else {}
+            W = torch.from_numpy(synth.gen_matrix(qt, N, K_, gm, **kw)).to(dev)
+            y = torch.empty(N, dtype=torch.float32, device=dev)
+            mats.append({"name": name, "type": qt, "N": N, "K": K_, "W": W, "stage": si, "y": y,
+                         "bytes": synth.matrix_bytes(qt, N, K_)})
+    return stages, mats, xs
+
+
+def record_step(kq, torch, mats, xs, stream, only_type=None):
+    for m in mats:
+        if only_type is not None and m["type"] != only_type:
+            continue
+        kq.kq_matvec(m["type"], m["W"], xs[m["stage"]], kq.KQ_BF16, m["y"], m["N"], m["K"], 1, stream)
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm the path once outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm = [float(r[0]) for r in self.rows if r and r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if len(r) > 1 and r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            for i, n in enumerate(names):
+                if len(r) > 3 + i and r[3 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(mats_host, seconds=12.0):
+    """The oracle (fp64 C, all host cores) on a bounded sample of the step's
+    matrices: whole matrices in decode order until ~`seconds` of CPU work."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    done_bytes, t0 = 0, time.perf_counter()
+    names = []
+    for (name, qt, N, K, W, x) in mats_host:
+        oracle.matvec(qt, W, N, K, x, threads=threads)
+        done_bytes += W.size
+        names.append(name)
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(names)} matrices of the step ({names[0]}..{names[-1]}), {done_bytes / 1e6:.1f} MB, {dt:.1f} s"}
+
+
+def host_sample(synth, n_mats=7, seed=0):
+    """The first layer's matrices (and inputs) on the host, for the CPU legs."""
+    out = []
+    for si, st in enumerate(synth.dense_layer_sweep()):
+        K = st[0][3]
+        x = synth.gen_x(1, K, synth.rng(seed, 1000 + si), "bf16")
+        for (name, qt, N, K_) in st:
+            gm = synth.rng(seed, 1000 + si, zlib.crc32(name.encode()) & 0xFFFF)
+            kw = {"q6_scale_range": (-32, 31)} if qt == synth.Q6_K else {}
+            out.append((name, qt, N, K_, synth.gen_matrix(qt, N, K_, gm, **kw), x))
+            if len(out) >= n_mats:
+                return out
+    return out
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the oracle itself (plain fp64 C on the host cores)."""
+    from gguf_quant_weight_super_gb300 import synth
+    if rank != 0:
+        return
+    sample = host_sample(synth, n_mats=4)
+    total_bytes = sum(s[4].size for s in sample)
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    for _ in range(max(0, args.warmup)):
+        pass  # the oracle has no state to warm; warm-up steps would only burn CPU time
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for (name, qt, N, K, W, x) in sample:
+            oracle.matvec(qt, W, N, K, x, threads=threads)
+    dt = time.perf_counter() - t0
+    v = total_bytes * args.steps / dt / 1e9
+    line = {"metric": METRIC, "value": v, "unit": "GB/s", "impl": "reference", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD + " (bounded sample: first 4 matrices of layer 0 per step)",
+                       "l2": "inputs larger than L2 on the GPU arm"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"4 matrices of layer 0, {total_bytes / 1e6:.1f} MB per step"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from gguf_quant_weight_super_gb300 import build, kq, synth
+    build.build()
+    kq.lib()
+    torch.manual_seed(0)
+
+    stages, mats, xs = build_model(torch, synth, seed=rank)
+    total_bytes = sum(m["bytes"] for m in mats)
+    launches_per_step = len(mats)
+    stream = torch.cuda.Stream()
+
+    step_graph = capture(torch, lambda: record_step(kq, torch, mats, xs, stream), stream)
+    q4_graph = capture(torch, lambda: record_step(kq, torch, mats, xs, stream, only_type=synth.Q4_K), stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step_graph.replay()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                step_graph.replay()
+        e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert kq.kq_device_error() == 0, "device error word set"
+
+    # dominant kernel: the Q4_K products of one step, timed alone (same order, same chaining)
+    q4 = [m for m in mats if m["type"] == synth.Q4_K]
+    q4_bytes = sum(m["bytes"] for m in q4)
+    for _ in range(3):
+        q4_graph.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            q4_graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    q4_ms = e0.elapsed_time(e1) / args.steps
+    peak, peak_kind = load_peaks()
+    achieved = q4_bytes / (q4_ms * 1e-3) / 1e9 / 1   # GB/s over the Q4_K launches
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            tr = json.load(f)
+        if tr.get("kernel_build") == kq.build_id():
+            traffic = tr.get("q4k_dram_bytes_per_step", None)
+            if traffic is not None:
+                traffic = traffic / len(q4)
+    except Exception:
+        traffic = None
+
+    # end to end: per step, H2D of the step's inputs from pinned host memory,
+    # the step, and D2H of the logits (the step's result)
+    x_host = [x.cpu().pin_memory() for x in xs]
+    logits = mats[-1]["y"]
+    logits_host = torch.empty_like(logits, device="cpu").pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in x_host)
+    d2h = logits.numel() * logits.element_size()
+
+    def e2e_step():
+        for xd, xh in zip(xs, x_host):
+            xd.copy_(xh, non_blocking=True)
+        step_graph.replay()
+        logits_host.copy_(logits, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(host_sample(synth, n_mats=36))
+
+    if rank == 0:
+        gbs = total_bytes * world / (ms * 1e-3) / 1e9
+        line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "u8 codes x bf16 x, int32/fp32 accumulate", "data": "synthetic",
+                "tok_s_equiv": world * 1e3 / ms, "roofline_tok_s_equiv": peak * 1e9 / total_bytes,
+                "frac_of_hbm_peak": gbs / world / peak,
+                "config": {"workload": WORKLOAD, "weight_bytes_per_step": total_bytes,
+                           "launches_per_step": launches_per_step, "graph": "CUDA graph, programmatic dependent launch",
+                           "l2": "inputs larger than L2 (2.49 GB of weights per step, read once)",
+                           "parallelism": f"replicas x{world}"},
+                "roofline": {"bound": "hbm", "kernel": "gemv1_kernel<Q4_K> (all Q4_K products of a step)",
+                             "achieved": achieved, "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs",
+                             "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                             "launches": len(q4), "bytes_per_launch": q4_bytes / len(q4),
+                             "avg_launch_us": q4_ms * 1e3 / len(q4)},
+                "e2e": {"value": total_bytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "gpu_launches": launches_per_step * args.steps,
+                "clocks": clk.summary()}
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

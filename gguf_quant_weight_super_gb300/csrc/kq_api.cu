@@ -1,0 +1,137 @@
+// kq_api.cu -- the extern "C" entry points of libkq (declared in include/kq.h):
+// argument checks, kernel choice, launch, and the device error word.
+#include <cstdio>
+
+#include "../../include/kq.h"
+#include "kq_internal.h"
+
+namespace kq {
+
+// The library's device error word (one per device that loads the library).
+__device__ int g_device_error = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {0};
+int* g_err_ptr[kMaxDevices] = {nullptr};
+thread_local int t_last_cuda_error = 0;
+
+}  // namespace
+
+int current_device_id() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  return (dev >= 0 && dev < kMaxDevices) ? dev : 0;
+}
+
+int num_sms() {
+  const int dev = current_device_id();
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+int* device_error_ptr() {
+  const int dev = current_device_id();
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+static kq_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return KQ_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  return KQ_ERR_CUDA;
+}
+
+static bool valid_type(int t) { return t == KQ_Q4_K || t == KQ_Q5_K || t == KQ_Q6_K; }
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace kq
+
+using namespace kq;
+
+extern "C" {
+
+size_t kq_block_bytes(int type) { return valid_type(type) ? static_cast<size_t>(block_bytes_of(type)) : 0; }
+
+kq_status kq_unpack(int type, const void* blocks, int64_t n_blocks, uint8_t* codes, int8_t* scales, uint8_t* mins,
+                    uint16_t* d_bits, uint16_t* dmin_bits, kq_stream_t stream) {
+  if (!valid_type(type)) return KQ_ERR_TYPE;
+  if (n_blocks < 0) return KQ_ERR_ARG;
+  if (n_blocks == 0) return KQ_OK;
+  if (!blocks) return KQ_ERR_ARG;
+  if (!aligned(blocks, 16)) return KQ_ERR_ALIGN;
+  return cuda_status(launch_unpack(type, blocks, n_blocks, codes, scales, mins, d_bits, dmin_bits,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kq_status kq_dequant(int type, const void* blocks, float* out, int64_t n, kq_stream_t stream) {
+  if (!valid_type(type)) return KQ_ERR_TYPE;
+  if (n < 0) return KQ_ERR_ARG;
+  if (n % 256) return KQ_ERR_SHAPE;
+  if (n == 0) return KQ_OK;
+  if (!blocks || !out) return KQ_ERR_ARG;
+  if (!aligned(blocks, 16) || !aligned(out, 16)) return KQ_ERR_ALIGN;
+  return cuda_status(launch_dequant(type, blocks, out, n / 256, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kq_status kq_matvec(int type, const void* W, const void* x, int x_dtype, float* y, int64_t N, int64_t K, int64_t M,
+                    kq_stream_t stream) {
+  if (!valid_type(type)) return KQ_ERR_TYPE;
+  if (x_dtype != KQ_F32 && x_dtype != KQ_BF16) return KQ_ERR_ARG;
+  if (N < 0 || K < 0 || M < 0) return KQ_ERR_ARG;
+  if (M > 16) return KQ_ERR_UNSUPPORTED;
+  if (K % 32 || K > (int64_t(1) << 24)) return KQ_ERR_SHAPE;
+  if (N == 0 || M == 0) return KQ_OK;
+  if (!y) return KQ_ERR_ARG;
+  if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, sizeof(float) * N * M, reinterpret_cast<cudaStream_t>(stream)));
+  if (!W || !x) return KQ_ERR_ARG;
+  if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4)) return KQ_ERR_ALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int bf16 = (x_dtype == KQ_BF16);
+  cudaError_t e = cudaErrorNotSupported;
+  if (M == 1) e = launch_gemv1(type, W, x, bf16, y, N, static_cast<int>(K), st, true);
+  if (e == cudaErrorNotSupported)
+    e = launch_gemv_batched(type, W, x, bf16, y, N, static_cast<int>(K), static_cast<int>(M), st, true);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_status(e);
+}
+
+kq_status kq_device_error(int* code, int clear) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int));
+  if (e != cudaSuccess) return cuda_status(e);
+  if (clear && v) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  if (code) *code = v;
+  return v ? KQ_ERR_DEVICE : KQ_OK;
+}
+
+int kq_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* kq_status_string(kq_status s) {
+  switch (s) {
+    case KQ_OK: return "ok";
+    case KQ_ERR_ARG: return "invalid argument";
+    case KQ_ERR_TYPE: return "unknown block type";
+    case KQ_ERR_SHAPE: return "unsupported shape (K must be a multiple of 32; dequant n a multiple of 256)";
+    case KQ_ERR_UNSUPPORTED: return "unsupported size (M must be 1..16, top_k 1..32)";
+    case KQ_ERR_ALIGN: return "misaligned pointer";
+    case KQ_ERR_CUDA: return "CUDA error";
+    case KQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KQ_ERR_DEVICE: return "device error word set";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

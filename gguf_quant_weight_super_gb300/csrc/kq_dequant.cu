@@ -1,0 +1,118 @@
+// kq_dequant.cu -- block -> fp32 weights, and block -> integer fields.
+//
+// Dequantization without a product is the fallback the loader uses when packed
+// kernels are not available ("GGUF in transformers", sections "Load GGUF with
+// transformers" and "Fine-tune from a GGUF checkpoint": GgufConfig(dequantize=
+// True) expands the weights).  The integer unpack exposes the same in-register
+// decode the products use (kq_decode.cuh) so its codes and scales can be
+// compared bit for bit.
+//
+// Exactness: for Q4_K/Q5_K, d*sc (<= 17 significant bits), q and dmin*m are
+// exact in fp32, so w = fma(d*sc, q, -(dmin*m)) rounds once -- the correctly
+// rounded value of the exact weight.  For Q6_K, d*sc*(q-32) has at most 23
+// significant bits and is exact.
+#include "kq_internal.h"
+
+namespace kq {
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int GROUPS = THREADS / 8;  // one 8-lane group per block
+
+template <int QT>
+__global__ void __launch_bounds__(THREADS) dequant_kernel(const uint8_t* __restrict__ blocks, float* __restrict__ out,
+                                                          int64_t n_blocks) {
+  constexpr int BB = Fmt<QT>::BYTES;
+  constexpr int P = Fmt<QT>::P;
+  constexpr int L = Fmt<QT>::L;
+  const int j = threadIdx.x & 7;
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * GROUPS + (threadIdx.x >> 3); b < n_blocks;
+       b += static_cast<int64_t>(gridDim.x) * GROUPS) {
+    LaneFields<QT> fl;
+    lane_fields<QT>(blocks + b * BB, j, fl);
+    const float d = half_bits_to_float(fl.d_bits);
+    const float dmin = half_bits_to_float(fl.dmin_bits);
+    float* o = out + b * 256;
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const float dsc = d * static_cast<float>(fl.sc[p]);
+      const float mm = dmin * static_cast<float>(fl.m[p]);
+      float w[L];
+#pragma unroll
+      for (int i = 0; i < L; ++i) {
+        const float q = static_cast<float>(code_of<QT>(fl, p * L + i));
+        if constexpr (QT == T_Q6_K) w[i] = dsc * (q - 32.0f);
+        else w[i] = __fmaf_rn(dsc, q, -mm);
+      }
+      float* dst = o + part_pos<QT>(j, p);
+#pragma unroll
+      for (int i = 0; i < L; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(w[i], w[i + 1], w[i + 2], w[i + 3]);
+    }
+  }
+}
+
+template <int QT>
+__global__ void __launch_bounds__(THREADS) unpack_kernel(const uint8_t* __restrict__ blocks, int64_t n_blocks,
+                                                         uint8_t* codes, int8_t* scales, uint8_t* mins,
+                                                         uint16_t* d_bits, uint16_t* dmin_bits) {
+  constexpr int BB = Fmt<QT>::BYTES;
+  constexpr int P = Fmt<QT>::P;
+  constexpr int L = Fmt<QT>::L;
+  const int j = threadIdx.x & 7;
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * GROUPS + (threadIdx.x >> 3); b < n_blocks;
+       b += static_cast<int64_t>(gridDim.x) * GROUPS) {
+    LaneFields<QT> fl;
+    lane_fields<QT>(blocks + b * BB, j, fl);
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const int pos = part_pos<QT>(j, p);
+      if (codes)
+        for (int i = 0; i < L; ++i) codes[b * 256 + pos + i] = static_cast<uint8_t>(code_of<QT>(fl, p * L + i));
+      // scale index: 32-weight sub-block (Q4_K/Q5_K) or 16-weight (Q6_K)
+      const int si = (QT == T_Q6_K) ? pos / 16 : pos / 32;
+      if (scales) scales[b * 16 + si] = static_cast<int8_t>(fl.sc[p]);
+      if (mins && QT != T_Q6_K) mins[b * 8 + si] = static_cast<uint8_t>(fl.m[p]);
+    }
+    if (j == 0) {
+      if (d_bits) d_bits[b] = static_cast<uint16_t>(fl.d_bits);
+      if (dmin_bits) dmin_bits[b] = static_cast<uint16_t>(fl.dmin_bits);
+    }
+  }
+}
+
+int grid_for(int64_t n_blocks) {
+  const int64_t need = (n_blocks + GROUPS - 1) / GROUPS;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  return static_cast<int>(need < cap ? need : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(int qtype, const void* blocks, float* out, int64_t n_blocks, cudaStream_t stream) {
+  if (n_blocks == 0) return cudaSuccess;
+  const uint8_t* b = static_cast<const uint8_t*>(blocks);
+  const int grid = grid_for(n_blocks);
+  switch (qtype) {
+    case T_Q4_K: dequant_kernel<T_Q4_K><<<grid, THREADS, 0, stream>>>(b, out, n_blocks); break;
+    case T_Q5_K: dequant_kernel<T_Q5_K><<<grid, THREADS, 0, stream>>>(b, out, n_blocks); break;
+    case T_Q6_K: dequant_kernel<T_Q6_K><<<grid, THREADS, 0, stream>>>(b, out, n_blocks); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(int qtype, const void* blocks, int64_t n_blocks, uint8_t* codes, int8_t* scales,
+                          uint8_t* mins, uint16_t* d_bits, uint16_t* dmin_bits, cudaStream_t stream) {
+  if (n_blocks == 0) return cudaSuccess;
+  const uint8_t* b = static_cast<const uint8_t*>(blocks);
+  const int grid = grid_for(n_blocks);
+  switch (qtype) {
+    case T_Q4_K: unpack_kernel<T_Q4_K><<<grid, THREADS, 0, stream>>>(b, n_blocks, codes, scales, mins, d_bits, dmin_bits); break;
+    case T_Q5_K: unpack_kernel<T_Q5_K><<<grid, THREADS, 0, stream>>>(b, n_blocks, codes, scales, mins, d_bits, dmin_bits); break;
+    case T_Q6_K: unpack_kernel<T_Q6_K><<<grid, THREADS, 0, stream>>>(b, n_blocks, codes, scales, mins, d_bits, dmin_bits); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kq

@@ -1,0 +1,150 @@
+"""Thin Python binding of libkq's C ABI (include/kq.h): argument marshalling only.
+
+Every function named ``kq_*`` here calls the C function of the same name with
+the device pointers of the given torch tensors and the current CUDA stream;
+all computation happens in libkq's CUDA kernels.  There is no fallback: if
+libkq.so is missing or fails to load, importing the library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libkq.so")
+
+KQ_Q4_K, KQ_Q5_K, KQ_Q6_K = 1, 2, 3
+KQ_F32, KQ_BF16 = 0, 1
+KQ_OK = 0
+STATUS = {0: "KQ_OK", -1: "KQ_ERR_ARG", -2: "KQ_ERR_TYPE", -3: "KQ_ERR_SHAPE", -4: "KQ_ERR_UNSUPPORTED",
+          -5: "KQ_ERR_ALIGN", -6: "KQ_ERR_CUDA", -7: "KQ_ERR_WORKSPACE", -8: "KQ_ERR_DEVICE"}
+
+# exported symbols and their C signatures (kept in step with include/kq.h)
+_P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+SIGNATURES = {
+    "kq_block_bytes": (_SZ, [_I]),
+    "kq_unpack": (_I, [_I, _P, _I64, _P, _P, _P, _P, _P, _P]),
+    "kq_dequant": (_I, [_I, _P, _P, _I64, _P]),
+    "kq_matvec": (_I, [_I, _P, _P, _I, _P, _I64, _I64, _I64, _P]),
+    "kq_device_error": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
+    "kq_last_cuda_error": (_I, []),
+    "kq_status_string": (ctypes.c_char_p, [_I]),
+}
+
+
+def build_id() -> str:
+    """Hash of the kernel sources (identifies which code a profile was taken on)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(PKG, "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+class KQError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = _lib.kq_status_string(status).decode() if _lib is not None else ""
+        extra = ""
+        if status == -6 and _lib is not None:
+            extra = f" (cudaError {_lib.kq_last_cuda_error()})"
+        super().__init__(f"{fn}: {STATUS.get(status, status)} -- {msg}{extra}")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkq.so (built in-tree by ``gguf_quant_weight_super_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libkq.so not built ({LIB_PATH}); run gguf_quant_weight_super_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("libkq takes device tensors only")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn: str, status: int):
+    if status != KQ_OK:
+        raise KQError(fn, status)
+
+
+def kq_block_bytes(qtype: int) -> int:
+    return lib().kq_block_bytes(qtype)
+
+
+def kq_unpack(qtype, blocks, n_blocks, codes=None, scales=None, mins=None, d_bits=None, dmin_bits=None,
+              stream=None):
+    _check("kq_unpack", lib().kq_unpack(qtype, _ptr(blocks), n_blocks, _ptr(codes), _ptr(scales), _ptr(mins),
+                                        _ptr(d_bits), _ptr(dmin_bits), _stream(stream)))
+
+
+def kq_dequant(qtype, blocks, out, n, stream=None):
+    _check("kq_dequant", lib().kq_dequant(qtype, _ptr(blocks), _ptr(out), n, _stream(stream)))
+
+
+def kq_matvec(qtype, W, x, x_dtype, y, N, K, M, stream=None):
+    _check("kq_matvec", lib().kq_matvec(qtype, _ptr(W), _ptr(x), x_dtype, _ptr(y), N, K, M, _stream(stream)))
+
+
+def kq_device_error(clear: bool = False) -> int:
+    code = ctypes.c_int(0)
+    st = lib().kq_device_error(ctypes.byref(code), int(clear))
+    if st not in (KQ_OK, -8):
+        raise KQError("kq_device_error", st)
+    return code.value
+
+
+# ---------------------------------------------------------------------------
+# Convenience wrappers that allocate outputs with torch (still one C call each).
+# ---------------------------------------------------------------------------
+
+def x_dtype_of(x: torch.Tensor) -> int:
+    if x.dtype == torch.float32:
+        return KQ_F32
+    if x.dtype == torch.bfloat16:
+        return KQ_BF16
+    raise TypeError("x must be float32 or bfloat16")
+
+
+def matvec(qtype: int, W: torch.Tensor, x: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None):
+    """y = W x for x of shape (M, K) (or (K,)); returns fp32 (M, N)."""
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
+    kq_matvec(qtype, W, x2, x_dtype_of(x2), y, N, K, M)
+    return y
+
+
+def dequant(qtype: int, blocks: torch.Tensor, n: int) -> torch.Tensor:
+    out = torch.empty(n, dtype=torch.float32, device=blocks.device)
+    kq_dequant(qtype, blocks, out, n)
+    return out

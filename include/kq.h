@@ -1,0 +1,128 @@
+/*
+ * kq.h -- C ABI of libkq: decode-time products against GGUF k-quant weights
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (sources: page title, section):
+ *   "GGUF in transformers" (Hugging Face blog), "What is the GGUF file
+ *     format?": Q4_K_M checkpoints keep most tensors in 4-bit k-quants and the
+ *     sensitive ones in Q6_K; Q5_K_M and Q6_K are the larger variants.
+ *   same page, "Reusing ggml's Metal kernels": the quantization kernel reads
+ *     the packed weights directly for matrix operations, including only the
+ *     experts an MoE layer selected, instead of expanding the whole matrix
+ *     before each decode step.
+ *   same page, "Fine-tune from a GGUF checkpoint" / "Load GGUF with
+ *     transformers": the fallback that dequantizes weights (kq_dequant).
+ *   "ANE Fieldfare" README (Show HN page), "How it works": each token's router
+ *     picks 8 of 128 experts and a shared FFN runs for every token;
+ *     "Speculative decoding": verify blocks of up to 16 tokens, so products
+ *     run for M = 1..16 tokens at once.
+ *
+ * Block formats (256 weights each; little-endian; the byte layout is the
+ * public GGUF layout as this library reads it -- the pages do not print it):
+ *   KQ_Q4_K  144 B: d fp16 | dmin fp16 | 12 B: 8 six-bit scales, 8 six-bit
+ *            mins | 128 B 4-bit codes.   w = d*sc_j*q - dmin*m_j, j = 32-weight sub-block
+ *   KQ_Q5_K  176 B: as Q4_K with 32 B of 5th code bits before the codes (q in 0..31).
+ *   KQ_Q6_K  210 B: 128 B low nibbles | 64 B high bit pairs | 16 int8 scales | d fp16.
+ *            w = d*sc_j*(q - 32), j = 16-weight sub-block, q in 0..63
+ *
+ * Matrices: W has N rows; row n is ceil(K/256) consecutive blocks, rows are
+ * consecutive (no padding).  Weights at positions k >= K in a row's last block
+ * are not part of the matrix and are never used.  K must be a multiple of 32.
+ * x is M rows of K values (row-major, fp32 or bfloat16); y is M rows of N
+ * fp32 values (row-major).
+ *
+ * Memory and ownership: every pointer argument is a device pointer owned by
+ * the caller.  The library allocates nothing, keeps no per-call state and does
+ * not synchronize; work is enqueued on `stream` (0 = legacy default stream).
+ * W must be 16-byte aligned; its allocation must be readable up to the next
+ * 16-byte boundary past its last byte (always true for cudaMalloc and the
+ * PyTorch caching allocator).  x must be 16-byte aligned; y 4-byte aligned.
+ * Outputs must not overlap inputs.
+ *
+ * Ordering: kernels are launched with programmatic stream serialization.
+ * Before waiting for the preceding kernel on the stream they read only W
+ * (and the expert weights), so W must not be written by the immediately
+ * preceding kernel; x, y, ids and gates are accessed only after that kernel
+ * has completed.
+ *
+ * Errors: argument errors are returned before anything is enqueued.  A failed
+ * launch returns KQ_ERR_CUDA (the CUDA error is available from
+ * kq_last_cuda_error).  Kernels never trap: a problem found on the device
+ * (an expert id out of range, a bounded wait that expired) is recorded in the
+ * library's device error word, read with kq_device_error.
+ */
+#ifndef KQ_H
+#define KQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kq_stream_t; /* same type as cudaStream_t */
+
+typedef enum { KQ_Q4_K = 1, KQ_Q5_K = 2, KQ_Q6_K = 3 } kq_type;
+typedef enum { KQ_F32 = 0, KQ_BF16 = 1 } kq_dtype;
+
+typedef int kq_status;
+#define KQ_OK 0
+#define KQ_ERR_ARG (-1)         /* null pointer, negative size, bad dtype       */
+#define KQ_ERR_TYPE (-2)        /* unknown block type                           */
+#define KQ_ERR_SHAPE (-3)       /* K not a multiple of 32, n not a multiple of 256 */
+#define KQ_ERR_UNSUPPORTED (-4) /* M outside 1..16, top_k outside 1..32          */
+#define KQ_ERR_ALIGN (-5)       /* pointer alignment rule broken                 */
+#define KQ_ERR_CUDA (-6)        /* a CUDA call failed (see kq_last_cuda_error)   */
+#define KQ_ERR_WORKSPACE (-7)   /* workspace missing or too small                */
+#define KQ_ERR_DEVICE (-8)      /* the device error word was set (kq_device_error) */
+
+/* Bytes of one 256-weight block: 144, 176, 210; 0 for an unknown type. */
+size_t kq_block_bytes(int type);
+
+/*
+ * Integer fields of n_blocks consecutive blocks (the super-block unpacker the
+ * products use, exposed for inspection).  Any output may be NULL.
+ *   codes     [n_blocks][256] uint8: q (Q4_K 0..15, Q5_K 0..31, Q6_K 0..63, unbiased)
+ *   scales    [n_blocks][16]  int8 : Q4_K/Q5_K sc_0..sc_7 (0..63, entries 8..15
+ *                                    untouched); Q6_K sc_0..sc_15 (-128..127)
+ *   mins      [n_blocks][8]   uint8: Q4_K/Q5_K m_0..m_7 (untouched for Q6_K)
+ *   d_bits    [n_blocks]      fp16 bit pattern of d
+ *   dmin_bits [n_blocks]      fp16 bit pattern of dmin (untouched for Q6_K)
+ */
+kq_status kq_unpack(int type, const void *blocks, int64_t n_blocks, uint8_t *codes, int8_t *scales,
+                    uint8_t *mins, uint16_t *d_bits, uint16_t *dmin_bits, kq_stream_t stream);
+
+/*
+ * Dequantize n weights (n a multiple of 256) stored as n/256 consecutive
+ * blocks into fp32: out[i] = the exact weight rounded once to fp32.
+ * blocks: 16-byte aligned.  out: 16-byte aligned, n floats.
+ */
+kq_status kq_dequant(int type, const void *blocks, float *out, int64_t n, kq_stream_t stream);
+
+/*
+ * y[m][n] = sum_{k<K} w[n][k] * x[m][k] for m < M, n < N, dequantizing W on
+ * the fly (each weight byte is read from memory once per call).
+ *   x_dtype KQ_F32 or KQ_BF16; M in 1..16; K a multiple of 32.
+ * Accumulation is fp32; the summation order depends only on W's shape, so for
+ * the same W and x row, y[m] is bit-identical for every M.
+ */
+kq_status kq_matvec(int type, const void *W, const void *x, int x_dtype, float *y, int64_t N, int64_t K,
+                    int64_t M, kq_stream_t stream);
+
+/*
+ * Read the device error word (KQ_OK when clean); with clear != 0 also reset
+ * it.  Synchronizes the device.
+ */
+kq_status kq_device_error(int *code, int clear);
+
+/* Last CUDA error code seen by a failing call on this host thread (0 if none). */
+int kq_last_cuda_error(void);
+
+/* Text for a status code. */
+const char *kq_status_string(kq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KQ_H */

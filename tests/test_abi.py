@@ -1,0 +1,65 @@
+"""CPU checks of the C ABI: libkq builds for sm_103a, loads, exports every
+function include/kq.h declares, and rejects bad arguments before touching the
+GPU (these paths make no CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gguf_quant_weight_super_gb300 import build as kqbuild
+from gguf_quant_weight_super_gb300 import kq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(kq_[a-z0-9_]+)\s*\(", txt))
+    return names
+
+
+@pytest.fixture(scope="module")
+def L():
+    kqbuild.build()
+    return kq.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert {"kq_matvec", "kq_dequant", "kq_unpack", "kq_block_bytes"} <= names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(kq.SIGNATURES) >= names
+
+
+def test_block_bytes(L):
+    assert [L.kq_block_bytes(t) for t in (1, 2, 3)] == [144, 176, 210]
+    assert L.kq_block_bytes(0) == 0 and L.kq_block_bytes(9) == 0
+
+
+def test_status_strings(L):
+    for s in range(0, -9, -1):
+        assert L.kq_status_string(s)
+
+
+def test_argument_errors_without_gpu(L):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    assert L.kq_matvec(7, fake, fake, 0, fake, 4, 256, 1, None) == -2         # type
+    assert L.kq_matvec(1, fake, fake, 5, fake, 4, 256, 1, None) == -1         # x dtype
+    assert L.kq_matvec(1, fake, fake, 0, fake, 4, 250, 1, None) == -3         # K % 32
+    assert L.kq_matvec(1, fake, fake, 0, fake, 4, 256, 17, None) == -4        # M > 16
+    assert L.kq_matvec(1, fake, fake, 0, fake, -1, 256, 1, None) == -1        # N < 0
+    assert L.kq_matvec(1, fake, fake, 0, fake, 0, 256, 1, None) == 0          # empty: no-op
+    assert L.kq_matvec(1, None, fake, 0, fake, 4, 256, 1, None) == -1         # null W
+    assert L.kq_matvec(1, P(0x1001), fake, 0, fake, 4, 256, 1, None) == -5    # W alignment
+    assert L.kq_dequant(1, fake, fake, 100, None) == -3                        # n % 256
+    assert L.kq_dequant(3, fake, P(0x1004), 256, None) == -5                   # out alignment
+    assert L.kq_dequant(3, fake, fake, 0, None) == 0
+    assert L.kq_unpack(4, fake, 1, None, None, None, None, None, None) == -2
+    assert L.kq_unpack(1, fake, -1, None, None, None, None, None, None) == -1
