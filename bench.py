@@ -192,6 +192,26 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_single(args):
+    """One product of a given shape, `--steps` times (for profiler captures)."""
+    import torch
+    from gguf_quant_weight_super_gb300 import build, kq, synth
+    build.build()
+    spec = args.single.split(":")
+    qt = {"Q4_K": synth.Q4_K, "Q5_K": synth.Q5_K, "Q6_K": synth.Q6_K}[spec[0]]
+    N, K = (int(v) for v in spec[1].split("x"))
+    M = int(spec[2]) if len(spec) > 2 else 1
+    g = synth.rng(0, qt, N, K)
+    W = torch.from_numpy(synth.gen_matrix(qt, N, K, g)).cuda()
+    x = torch.from_numpy(synth.gen_x(M, K, g, "bf16").view(np.int16)).cuda().view(torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    for _ in range(args.steps):
+        kq.kq_matvec(qt, W, x, kq.KQ_BF16, y, N, K, M)
+    torch.cuda.synchronize()
+    assert kq.kq_device_error() == 0
+    print(json.dumps({"single": args.single, "runs": args.steps, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -199,7 +219,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single", default=None,
+                    help="profiling helper: run one product TYPE:NxK[:M] (e.g. Q4_K:19456x2560) --steps times")
     args = ap.parse_args()
+    if args.single:
+        run_single(args)
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -272,9 +297,9 @@ def main():
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             tr = json.load(f)
         if tr.get("kernel_build") == kq.build_id():
-            traffic = tr.get("q4k_dram_bytes_per_step", None)
-            if traffic is not None:
-                traffic = traffic / len(q4)
+            # DRAM bytes per launch from one ncu capture (ratio to the weight
+            # bytes), scaled to the average Q4_K launch of the step
+            traffic = tr["q4k_dram_bytes_ratio"] * q4_bytes / len(q4)
     except Exception:
         traffic = None
 

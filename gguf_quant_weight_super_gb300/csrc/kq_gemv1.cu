@@ -54,6 +54,9 @@ namespace {
 #ifndef KQ_G1_SMEM_CAP
 #define KQ_G1_SMEM_CAP (227 * 1024)
 #endif
+#ifndef KQ_G1_ROWCONTIG_MAXNB
+#define KQ_G1_ROWCONTIG_MAXNB 16
+#endif
 
 constexpr int NW = KQ_G1_NW;        // warps per CTA
 constexpr int SMAX = KQ_G1_SMAX;    // ring stages per warp (at most)
@@ -95,6 +98,7 @@ struct G1Args {
   int S;              // ring stages per warp
   int KC;             // blocks per stage
   int srb;            // bytes per row inside a stage
+  int rowcontig;      // a stage holds whole rows: one copy of TR consecutive rows
   int stage_bytes;
   int64_t ntiles;
   int tiles_per_cta;
@@ -350,6 +354,20 @@ __device__ __forceinline__ uint32_t seg_of(const G1Args& a, int64_t row, int b0,
 template <int BB>
 __device__ __forceinline__ void issue_stage(const G1Args& a, int64_t tile, int b0, int nblk, uint8_t* slot,
                                             uint64_t* bar, int lane) {
+  if (a.rowcontig) {  // whole rows: the tile's rows are one contiguous byte range
+    if (lane == 0) {
+      const int64_t r0 = tile * TR;
+      const int64_t nrows = min_i64(TR, a.N - r0);
+      const uintptr_t s0 = reinterpret_cast<uintptr_t>(a.W + r0 * a.row_bytes);
+      const uintptr_t e0 = s0 + static_cast<uintptr_t>(nrows * a.row_bytes);
+      const uintptr_t as = s0 & ~uintptr_t(15), ae = (e0 + 15) & ~uintptr_t(15);
+      const uint32_t len = static_cast<uint32_t>(ae - as);
+      mbar_arrive_expect_tx(bar, len);
+      bulk_g2s(slot, reinterpret_cast<const uint8_t*>(as), len, bar);
+    }
+    __syncwarp();
+    return;
+  }
   const int64_t row = tile * TR + lane;
   const bool mine = lane < TR && row < a.N;
   const uint8_t* src = nullptr;
@@ -452,9 +470,14 @@ __global__ void __launch_bounds__(NW * 32, MINB) gemv1_kernel(const G1Args a) {
           const int lr = rs + 2 * k;
           const int64_t row = tile * TR + lr;
           rok[k] = row < a.N;
-          const uintptr_t s0 = reinterpret_cast<uintptr_t>(a.W + row * a.row_bytes +
-                                                           static_cast<int64_t>(rb0 + cb) * BB);
-          rowp[k] = sp + lr * a.srb + (s0 & 15);
+          if (a.rowcontig) {
+            const uintptr_t s0 = reinterpret_cast<uintptr_t>(a.W + tile * TR * a.row_bytes);
+            rowp[k] = sp + (s0 & 15) + lr * a.row_bytes;
+          } else {
+            const uintptr_t s0 = reinterpret_cast<uintptr_t>(a.W + row * a.row_bytes +
+                                                             static_cast<int64_t>(rb0 + cb) * BB);
+            rowp[k] = sp + lr * a.srb + (s0 & 15);
+          }
         }
         for (int sb = 0; sb < n; sb += 4) {
           const int bi = sb + bs;           // block of this quad within the stage
@@ -592,10 +615,25 @@ cudaError_t launch_gemv1(int qtype, const void* W, const void* x, int x_bf16, fl
   a.nr = (a.nb + KB - 1) / KB;
   const int NL = x_bf16 ? 2 : 3;
   if (a.nb * 64 > 16 * NW * 32) return cudaErrorNotSupported;  // x words per thread (stage_x)
-  // ring: largest stage (up to 8 blocks) and depth that fit
+  // ring: whole-row stages (one copy per stage) when they fit, else row
+  // segments of up to KCMAX blocks; deepest ring that fits
   const int slack = (qtype == T_Q6_K) ? 32 : 0;
   size_t smem = 0;
   bool fit = false;
+  if (a.nr == 1 && a.nb <= KQ_G1_ROWCONTIG_MAXNB) {
+    const int stage = static_cast<int>(((TR * a.row_bytes + 32 + 15) / 16) * 16);
+    for (int S = SMAX; S >= 2 && !fit; --S) {
+      smem = g1_smem(a.nb, NL, S, stage, 1, a.tiles_per_cta);
+      if (smem <= static_cast<size_t>(SMEM_CAP)) {
+        a.KC = a.nb;
+        a.S = S;
+        a.srb = static_cast<int>(a.row_bytes);
+        a.stage_bytes = stage;
+        a.rowcontig = 1;
+        fit = true;
+      }
+    }
+  }
   for (int kc = (KB < KCMAX ? KB : KCMAX); kc >= 4 && !fit; kc -= 4) {
     for (int S = SMAX; S >= 2 && !fit; --S) {
       int srb = (kc * BB + slack + 15) & ~15;
