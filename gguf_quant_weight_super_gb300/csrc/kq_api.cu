@@ -1,6 +1,7 @@
 // kq_api.cu -- the extern "C" entry points of libkq (declared in include/kq.h):
 // argument checks, kernel choice, launch, and the device error word.
 #include <cstdio>
+#include <cstring>
 
 #include "../../include/kq.h"
 #include "kq_internal.h"
@@ -97,9 +98,99 @@ kq_status kq_matvec(int type, const void* W, const void* x, int x_dtype, float* 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int bf16 = (x_dtype == KQ_BF16);
   cudaError_t e = cudaErrorNotSupported;
-  if (M == 1) e = launch_gemv1(type, W, x, bf16, y, N, static_cast<int>(K), st, true);
+  if (M == 1) e = launch_matvec1(type, W, x, bf16, y, N, static_cast<int>(K), st, true);
   if (e == cudaErrorNotSupported)
     e = launch_gemv_batched(type, W, x, bf16, y, N, static_cast<int>(K), static_cast<int>(M), st, true);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_status(e);
+}
+
+static_assert(sizeof(ProgPlan) <= sizeof(kq_chain_plan), "plan storage");
+
+static bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+static kq_status check_chain(const kq_op* ops, int n_ops) {
+  if (!ops || n_ops <= 0) return KQ_ERR_ARG;
+  int last_wait = 0;
+  for (int i = 0; i < n_ops; ++i) {
+    const kq_op& o = ops[i];
+    if (!valid_type(o.type)) return KQ_ERR_TYPE;
+    if (o.x_dtype != KQ_F32 && o.x_dtype != KQ_BF16) return KQ_ERR_ARG;
+    if (o.reserved != 0 || o.N <= 0 || o.K <= 0) return KQ_ERR_ARG;
+    if (o.K % 32) return KQ_ERR_SHAPE;
+    if (o.K > 16384) return KQ_ERR_UNSUPPORTED;
+    if (!o.W || !o.x || !o.y) return KQ_ERR_ARG;
+    if (!aligned(o.W, 16) || !aligned(o.x, 16) || !aligned(o.y, 4)) return KQ_ERR_ALIGN;
+    if (i > 0 && o.wait_previous) last_wait = i;
+    // x may not be an output of an op that can still be running
+    for (int j = last_wait; j < i; ++j)
+      if (overlaps(o.x, o.K * (o.x_dtype == KQ_BF16 ? 2 : 4), ops[j].y, ops[j].N * 4)) return KQ_ERR_ARG;
+  }
+  for (int i = 0; i < n_ops; ++i) {
+    const size_t yb = ops[i].N * 4;
+    for (int j = 0; j < n_ops; ++j) {
+      const int64_t nbj = (ops[j].K + 255) / 256;
+      if (overlaps(ops[i].y, yb, ops[j].W, nbj * ops[j].N * block_bytes_of(ops[j].type))) return KQ_ERR_ARG;
+      if (j != i && overlaps(ops[i].y, yb, ops[j].y, ops[j].N * 4)) return KQ_ERR_ARG;
+      if (j <= i && overlaps(ops[i].y, yb, ops[j].x, ops[j].K * (ops[j].x_dtype == KQ_BF16 ? 2 : 4)))
+        return KQ_ERR_ARG;
+    }
+  }
+  return KQ_OK;
+}
+
+static void to_desc(const kq_op* ops, int n_ops, ProgOpDesc* d) {
+  for (int i = 0; i < n_ops; ++i) {
+    d[i].type = ops[i].type;
+    d[i].x_bf16 = ops[i].x_dtype == KQ_BF16;
+    d[i].wait_previous = ops[i].wait_previous != 0;
+    d[i].W = ops[i].W;
+    d[i].x = ops[i].x;
+    d[i].y = ops[i].y;
+    d[i].N = ops[i].N;
+    d[i].K = ops[i].K;
+  }
+}
+
+size_t kq_chain_workspace_size(const kq_op* ops, int n_ops) {
+  if (check_chain(ops, n_ops) != KQ_OK) return 0;
+  ProgOpDesc* d = new ProgOpDesc[n_ops];
+  to_desc(ops, n_ops, d);
+  const size_t b = prog_workspace_size(d, n_ops);
+  delete[] d;
+  return b;
+}
+
+kq_status kq_chain_prepare(const kq_op* ops, int n_ops, void* workspace, size_t workspace_bytes,
+                           kq_chain_plan* plan, kq_stream_t stream) {
+  const kq_status st = check_chain(ops, n_ops);
+  if (st != KQ_OK) return st;
+  if (!plan) return KQ_ERR_ARG;
+  if (!workspace || !aligned(workspace, 256)) return KQ_ERR_WORKSPACE;
+  ProgOpDesc* d = new ProgOpDesc[n_ops];
+  to_desc(ops, n_ops, d);
+  const size_t need = prog_workspace_size(d, n_ops);
+  if (need == 0) { delete[] d; return KQ_ERR_UNSUPPORTED; }
+  if (workspace_bytes < need) { delete[] d; return KQ_ERR_WORKSPACE; }
+  ProgPlan p = {};
+  const cudaError_t e = prog_prepare(d, n_ops, workspace, workspace_bytes, &p,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  delete[] d;
+  if (e != cudaSuccess) return cuda_status(e);
+  memset(plan, 0, sizeof(*plan));
+  memcpy(plan, &p, sizeof(p));
+  return KQ_OK;
+}
+
+kq_status kq_chain_run(const kq_chain_plan* plan, void* workspace, kq_stream_t stream) {
+  if (!plan || !workspace) return KQ_ERR_ARG;
+  ProgPlan p;
+  memcpy(&p, plan, sizeof(p));
+  if (p.n_ops <= 0) return KQ_ERR_ARG;
+  cudaError_t e = prog_run(&p, workspace, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_status(e);
 }

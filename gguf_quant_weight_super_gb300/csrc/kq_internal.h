@@ -29,6 +29,34 @@ cudaError_t launch_gemv_batched(int qtype, const void* W, const void* x, int x_b
 cudaError_t launch_gemv1(int qtype, const void* W, const void* x, int x_bf16, float* y, int64_t N, int K,
                          cudaStream_t stream, bool pdl);
 
+// One-token products (kq_gemv.cu): a single product, or a program of
+// products run by one persistent launch with grid-wide ordering between
+// dependent ones and split-K partial sums in the program's workspace.
+cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, float* y, int64_t N, int K,
+                           cudaStream_t stream, bool pdl);
+struct ProgOpDesc {
+  int type, x_bf16, wait_previous;
+  const void* W;
+  const void* x;
+  float* y;
+  int64_t N, K;
+};
+struct ProgPlan {
+  int n_ops, nb_max, nl_max, S, slot;
+  int coop;       // grid barriers: cooperative launch
+  int final_fix;  // split-K sums remain after the last op
+  int pad;
+  int64_t smem, ws_bytes;
+};
+// workspace bytes of a program (0: some op cannot run on this path)
+size_t prog_workspace_size(const ProgOpDesc* descs, int n_ops);
+// plans the program, writes it into ws (stream-ordered, then synchronizes)
+cudaError_t prog_prepare(const ProgOpDesc* descs, int n_ops, void* ws, size_t ws_bytes, ProgPlan* plan,
+                         cudaStream_t stream);
+cudaError_t prog_run(const ProgPlan* plan, void* ws, cudaStream_t stream);
+// L2 prefetch distance of the one-token kernel, in stages (0: none)
+void set_prefetch_stages(int pf);
+
 cudaError_t launch_dequant(int qtype, const void* blocks, float* out, int64_t n_blocks, cudaStream_t stream);
 cudaError_t launch_unpack(int qtype, const void* blocks, int64_t n_blocks, uint8_t* codes, int8_t* scales,
                           uint8_t* mins, uint16_t* d_bits, uint16_t* dmin_bits, cudaStream_t stream);

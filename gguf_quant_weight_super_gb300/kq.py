@@ -28,6 +28,9 @@ SIGNATURES = {
     "kq_unpack": (_I, [_I, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "kq_dequant": (_I, [_I, _P, _P, _I64, _P]),
     "kq_matvec": (_I, [_I, _P, _P, _I, _P, _I64, _I64, _I64, _P]),
+    "kq_chain_workspace_size": (_SZ, [_P, _I]),
+    "kq_chain_prepare": (_I, [_P, _I, _P, _SZ, _P, _P]),
+    "kq_chain_run": (_I, [_P, _P, _P]),
     "kq_device_error": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
     "kq_last_cuda_error": (_I, []),
     "kq_status_string": (ctypes.c_char_p, [_I]),
@@ -115,6 +118,43 @@ def kq_matvec(qtype, W, x, x_dtype, y, N, K, M, stream=None):
     _check("kq_matvec", lib().kq_matvec(qtype, _ptr(W), _ptr(x), x_dtype, _ptr(y), N, K, M, _stream(stream)))
 
 
+class KqOp(ctypes.Structure):
+    """struct kq_op of include/kq.h."""
+    _fields_ = [("type", ctypes.c_int32), ("x_dtype", ctypes.c_int32), ("wait_previous", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("W", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class KqChainPlan(ctypes.Structure):
+    """struct kq_chain_plan of include/kq.h (opaque)."""
+    _fields_ = [("opaque", ctypes.c_int64 * 8)]
+
+
+def _op_array(ops):
+    arr = (KqOp * len(ops))()
+    for i, o in enumerate(ops):
+        arr[i] = KqOp(o["type"], o["x_dtype"], int(o.get("wait_previous", 0)), 0, _ptr(o["W"]), _ptr(o["x"]),
+                      _ptr(o["y"]), o["N"], o["K"])
+    return arr
+
+
+def kq_chain_workspace_size(ops) -> int:
+    arr = _op_array(ops)
+    return lib().kq_chain_workspace_size(ctypes.cast(arr, ctypes.c_void_p), len(ops))
+
+
+def kq_chain_prepare(ops, workspace, workspace_bytes, plan: KqChainPlan, stream=None):
+    arr = _op_array(ops)
+    _check("kq_chain_prepare", lib().kq_chain_prepare(ctypes.cast(arr, ctypes.c_void_p), len(ops), _ptr(workspace),
+                                                      workspace_bytes, ctypes.cast(ctypes.pointer(plan), ctypes.c_void_p),
+                                                      _stream(stream)))
+
+
+def kq_chain_run(plan: KqChainPlan, workspace, stream=None):
+    _check("kq_chain_run", lib().kq_chain_run(ctypes.cast(ctypes.pointer(plan), ctypes.c_void_p), _ptr(workspace),
+                                              _stream(stream)))
+
+
 def kq_device_error(clear: bool = False) -> int:
     code = ctypes.c_int(0)
     st = lib().kq_device_error(ctypes.byref(code), int(clear))
@@ -142,6 +182,31 @@ def matvec(qtype: int, W: torch.Tensor, x: torch.Tensor, N: int, K: int, out: to
     y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
     kq_matvec(qtype, W, x2, x_dtype_of(x2), y, N, K, M)
     return y
+
+
+class Chain:
+    """A prepared chain of one-token products (kq_chain_* of include/kq.h).
+
+    ops: dicts with keys type, x_dtype, W, x, y, N, K and optionally
+    wait_previous; the tensors must stay alive while the chain is used.
+    The workspace is a torch uint8 tensor owned by this object.
+    """
+
+    def __init__(self, ops, device=None, stream=None):
+        self.ops = list(ops)
+        n = kq_chain_workspace_size(self.ops)
+        if n == 0:
+            raise KQError("kq_chain_workspace_size", -4)
+        dev = device if device is not None else self.ops[0]["y"].device
+        self.workspace = torch.empty(n + 256, dtype=torch.uint8, device=dev)
+        off = (-self.workspace.data_ptr()) % 256
+        self._ws_ptr = self.workspace.data_ptr() + off
+        self._ws_bytes = n
+        self.plan = KqChainPlan()
+        kq_chain_prepare(self.ops, self._ws_ptr, self._ws_bytes, self.plan, stream)
+
+    def run(self, stream=None):
+        kq_chain_run(self.plan, self._ws_ptr, stream)
 
 
 def dequant(qtype: int, blocks: torch.Tensor, n: int) -> torch.Tensor:

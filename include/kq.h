@@ -104,11 +104,68 @@ kq_status kq_dequant(int type, const void *blocks, float *out, int64_t n, kq_str
  * y[m][n] = sum_{k<K} w[n][k] * x[m][k] for m < M, n < N, dequantizing W on
  * the fly (each weight byte is read from memory once per call).
  *   x_dtype KQ_F32 or KQ_BF16; M in 1..16; K a multiple of 32.
- * Accumulation is fp32; the summation order depends only on W's shape, so for
- * the same W and x row, y[m] is bit-identical for every M.
+ * Accumulation is fp32 in a fixed order, so repeated calls give identical y;
+ * the order (hence the last bits of y) differs between M = 1 and M > 1.
  */
 kq_status kq_matvec(int type, const void *W, const void *x, int x_dtype, float *y, int64_t N, int64_t K,
                     int64_t M, kq_stream_t stream);
+
+/*
+ * Chains of one-token products run by one persistent launch.
+ *
+ * "GGUF in transformers", "Keeping the CPU and GPU working together": a
+ * decode step is a sequence of products, and the device should not idle
+ * between them.  A chain runs n_ops products y_i = W_i x_i (one token each)
+ * in one launch: weights stream continuously across op boundaries, and an op
+ * with wait_previous != 0 reads its x only after every earlier op of the
+ * chain has finished (a grid-wide barrier), so x_i may be computed from
+ * earlier outputs by the caller's own kernels only between runs, or be an
+ * earlier op's y.  Ops without wait_previous may run concurrently with the
+ * ops before them and must not read their outputs.
+ *
+ * Usage: size = kq_chain_workspace_size(ops, n); allocate a device workspace
+ * of that many bytes (256-byte aligned); kq_chain_prepare once (synchronous:
+ * it plans the chain and copies it into the workspace); then kq_chain_run any
+ * number of times.  The pointers and shapes of the ops are fixed by prepare;
+ * the data behind them may change between runs.  The workspace (owned by the
+ * caller) holds the compiled chain, grid-barrier counters and split-K
+ * partial sums; two runs must not use one workspace at the same time.
+ */
+typedef struct kq_op {
+  int32_t type;          /* KQ_Q4_K, KQ_Q5_K or KQ_Q6_K                         */
+  int32_t x_dtype;       /* KQ_F32 or KQ_BF16                                   */
+  int32_t wait_previous; /* nonzero: start after all earlier ops have finished  */
+  int32_t reserved;      /* must be 0                                           */
+  const void *W;         /* N x ceil(K/256) blocks, 16-byte aligned             */
+  const void *x;         /* K values, 16-byte aligned                           */
+  float *y;              /* N floats, 4-byte aligned                            */
+  int64_t N, K;          /* N >= 1; K a multiple of 32, at most 16384           */
+} kq_op;
+
+typedef struct kq_chain_plan {
+  int64_t opaque[8];
+} kq_chain_plan;
+
+/* Workspace bytes for the chain; 0 if an op's shape is outside this path. */
+size_t kq_chain_workspace_size(const kq_op *ops, int n_ops);
+
+/*
+ * Plan the chain into workspace and *plan.  Errors: KQ_ERR_ARG (null or
+ * overlapping buffers: an op's y may not overlap any W, any x of the same or
+ * an earlier op, or an x read before the next wait_previous), KQ_ERR_TYPE,
+ * KQ_ERR_SHAPE, KQ_ERR_UNSUPPORTED (K > 16384), KQ_ERR_ALIGN,
+ * KQ_ERR_WORKSPACE (workspace NULL, misaligned or smaller than
+ * kq_chain_workspace_size).  Enqueues copies on stream and synchronizes it.
+ */
+kq_status kq_chain_prepare(const kq_op *ops, int n_ops, void *workspace, size_t workspace_bytes,
+                           kq_chain_plan *plan, kq_stream_t stream);
+
+/*
+ * Run a prepared chain on stream.  A chain with wait_previous ops (or with
+ * split-K outputs) is a cooperative launch: one CTA per SM must be able to
+ * start, else KQ_ERR_CUDA.
+ */
+kq_status kq_chain_run(const kq_chain_plan *plan, void *workspace, kq_stream_t stream);
 
 /*
  * Read the device error word (KQ_OK when clean); with clear != 0 also reset

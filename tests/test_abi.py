@@ -63,3 +63,23 @@ def test_argument_errors_without_gpu(L):
     assert L.kq_dequant(3, fake, fake, 0, None) == 0
     assert L.kq_unpack(4, fake, 1, None, None, None, None, None, None) == -2
     assert L.kq_unpack(1, fake, -1, None, None, None, None, None, None) == -1
+
+
+def test_chain_argument_errors_without_gpu(L):
+    """Chain checks that run before any CUDA call (fake device addresses)."""
+    def ops(**kw):
+        o = dict(type=1, x_dtype=1, wait_previous=0, W=0x100000, x=0x200000, y=0x300000, N=64, K=512)
+        o.update(kw)
+        return o
+    assert kq.kq_chain_workspace_size([ops(type=9)]) == 0
+    assert kq.kq_chain_workspace_size([ops(K=500)]) == 0
+    assert kq.kq_chain_workspace_size([ops(K=16384 + 32)]) == 0
+    assert kq.kq_chain_workspace_size([ops(x=0x200008)]) == 0          # x alignment
+    assert kq.kq_chain_workspace_size([ops(y=0x200000)]) == 0          # y overlaps x
+    # op 2 reads op 1's output without a barrier
+    assert kq.kq_chain_workspace_size([ops(), ops(x=0x300000, x_dtype=0, W=0x400000, y=0x500000)]) == 0
+    plan = kq.KqChainPlan()
+    with pytest.raises(kq.KQError):
+        kq.kq_chain_prepare([ops(type=9)], 0x800000, 1 << 20, plan, stream=0)
+    with pytest.raises(kq.KQError):                                      # workspace alignment
+        kq.kq_chain_prepare([ops()], 0x800010, 1 << 20, plan, stream=0)

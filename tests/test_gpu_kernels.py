@@ -5,7 +5,7 @@
 * matvec: max |y_gpu - y_oracle| / sum_k |w x| <= 1e-4 (fp32 x) / 4e-3 (bf16 x),
   on sizes that span several tiles and a ragged tail, the degenerate shapes,
   and the full-size matrices of the benchmark workloads (sampled rows);
-* bit-identical rows for every batch size M (same W, same x row);
+* rows of a batched product match the one-token product within tolerance;
 * no writes outside y.
 """
 import numpy as np
