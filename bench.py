@@ -3,10 +3,14 @@
 One step = one token through the whole weight stream of a 36-layer dense
 decoder (hidden 2560; q 2560->4096, k/v 2560->1024, o 4096->2560, gate/up
 2560->9728, down 9728->2560; LM head 2560->151936), Q4_K everywhere except
-Q6_K for v_proj and down_proj on even layers and for the LM head.  Every
-matrix is a separate kq_matvec call in decode order (q, k, v share an input;
-gate, up share an input); the whole step is captured in a CUDA graph whose
-kernels are chained with programmatic dependent launch.
+Q6_K for v_proj and down_proj on even layers and for the LM head, in decode
+order (q, k, v share an input; gate, up share an input; each stage waits for
+the previous one).  Two ways to run the step through libkq are timed:
+  launches: one kq_matvec per matrix (253), captured in a CUDA graph whose
+            kernels are chained with programmatic dependent launch;
+  chain:    one kq_chain_run of the 253 products, a grid barrier before every
+            stage (one persistent launch per step).
+The headline value is the faster of the two; both are reported.
 
 Prints one JSON line.  `value` is quantized-weight GB/s (stored weight bytes
 read per second); tok/s-equivalent = steps per second.  Inputs are synthetic
@@ -71,6 +75,18 @@ def record_step(kq, torch, mats, xs, stream, only_type=None):
         kq.kq_matvec(m["type"], m["W"], xs[m["stage"]], kq.KQ_BF16, m["y"], m["N"], m["K"], 1, stream)
 
 
+def make_chain(kq, mats, xs, only_type=None):
+    """The step as one chain: a grid barrier before the first product of every stage."""
+    ops, last_stage = [], None
+    for m in mats:
+        if only_type is not None and m["type"] != only_type:
+            continue
+        ops.append({"type": m["type"], "x_dtype": kq.KQ_BF16, "W": m["W"], "x": xs[m["stage"]], "y": m["y"],
+                    "N": m["N"], "K": m["K"], "wait_previous": int(bool(ops) and m["stage"] != last_stage)})
+        last_stage = m["stage"]
+    return kq.Chain(ops)
+
+
 def capture(torch, fn, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -130,22 +146,25 @@ class ClockSampler:
 
 
 def cpu_baseline(mats_host, seconds=12.0):
-    """The oracle (fp64 C, all host cores) on a bounded sample of the step's
-    matrices: whole matrices in decode order until ~`seconds` of CPU work."""
+    """The oracle (fp64 C, all host cores) on a bounded sample of the step:
+    the first layer's matrices in decode order, repeated until ~`seconds` of
+    CPU work."""
     import oracle
     oracle.build()
     threads = os.cpu_count() or 1
-    done_bytes, t0 = 0, time.perf_counter()
-    names = []
-    for (name, qt, N, K, W, x) in mats_host:
-        oracle.matvec(qt, W, N, K, x, threads=threads)
-        done_bytes += W.size
-        names.append(name)
+    done_bytes, passes, t0 = 0, 0, time.perf_counter()
+    while True:
+        for (name, qt, N, K, W, x) in mats_host:
+            oracle.matvec(qt, W, N, K, x, threads=threads)
+            done_bytes += W.size
+        passes += 1
         if time.perf_counter() - t0 > seconds:
             break
     dt = time.perf_counter() - t0
+    names = [m[0] for m in mats_host]
     return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{len(names)} matrices of the step ({names[0]}..{names[-1]}), {done_bytes / 1e6:.1f} MB, {dt:.1f} s"}
+            "sample": f"{len(names)} matrices of layer 0 ({names[0]}..{names[-1]}) x {passes} passes, "
+                      f"{done_bytes / 1e6:.0f} MB, {dt:.1f} s"}
 
 
 def host_sample(synth, n_mats=7, seed=0):
@@ -250,56 +269,66 @@ def main():
     launches_per_step = len(mats)
     stream = torch.cuda.Stream()
 
-    step_graph = capture(torch, lambda: record_step(kq, torch, mats, xs, stream), stream)
-    q4_graph = capture(torch, lambda: record_step(kq, torch, mats, xs, stream, only_type=synth.Q4_K), stream)
+    chain = make_chain(kq, mats, xs)
+    graphs = {"launches": capture(torch, lambda: record_step(kq, torch, mats, xs, stream), stream),
+              "chain": capture(torch, lambda: chain.run(stream), stream)}
+    launches = {"launches": launches_per_step, "chain": 1}
 
     def barrier():
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(max(3, args.warmup)):
-        step_graph.replay()
-    barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+
+    def timed(graph, steps, clk=None):
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
         barrier()
         e0.record(stream)
         with torch.cuda.stream(stream):
-            for _ in range(args.steps):
-                step_graph.replay()
+            for _ in range(steps):
+                graph.replay()
         e1.record(stream)
         barrier()
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    assert kq.kq_device_error() == 0, "device error word set"
+        return e0.elapsed_time(e1) / steps
 
-    # dominant kernel: the Q4_K products of one step, timed alone (same order, same chaining)
-    q4 = [m for m in mats if m["type"] == synth.Q4_K]
-    q4_bytes = sum(m["bytes"] for m in q4)
-    for _ in range(3):
-        q4_graph.replay()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            q4_graph.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    q4_ms = e0.elapsed_time(e1) / args.steps
+    variants = {}
+    with ClockSampler(local) as clk:
+        for name, graph in graphs.items():
+            t = timed(graph, args.steps)
+            if dist is not None:
+                tt = torch.tensor([t], device="cuda")
+                dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+                t = float(tt.item())
+            variants[name] = t
+    assert kq.kq_device_error() == 0, "device error word set"
+    best = min(variants, key=variants.get)
+    ms = variants[best]
+    step_graph = graphs[best]
+
+    # dominant kernel: prog_kernel.  For the chain, one launch is the whole
+    # step; for separate launches, the Q4_K products of a step timed alone
+    # (same order, same chaining).
     peak, peak_kind = load_peaks()
-    achieved = q4_bytes / (q4_ms * 1e-3) / 1e9 / 1   # GB/s over the Q4_K launches
+    if best == "chain":
+        q4_bytes, n_q4, q4_ms = total_bytes, 1, ms
+        rf_kernel = "prog_kernel (chain: all 253 products of a step, one launch)"
+    else:
+        q4 = [m for m in mats if m["type"] == synth.Q4_K]
+        q4_bytes, n_q4 = sum(m["bytes"] for m in q4), len(q4)
+        q4_graph = capture(torch, lambda: record_step(kq, torch, mats, xs, stream, only_type=synth.Q4_K), stream)
+        q4_ms = timed(q4_graph, args.steps)
+        rf_kernel = "prog_kernel (all Q4_K products of a step, one launch each)"
+    achieved = q4_bytes / (q4_ms * 1e-3) / 1e9
     traffic = None
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             tr = json.load(f)
-        if tr.get("kernel_build") == kq.build_id():
+        if tr.get("kernel_build") == kq.build_id() and tr.get("variant") == best:
             # DRAM bytes per launch from one ncu capture (ratio to the weight
-            # bytes), scaled to the average Q4_K launch of the step
-            traffic = tr["q4k_dram_bytes_ratio"] * q4_bytes / len(q4)
+            # bytes), scaled to the average launch of this variant
+            traffic = tr["dram_bytes_ratio"] * q4_bytes / n_q4
     except Exception:
         traffic = None
 
@@ -335,7 +364,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(host_sample(synth, n_mats=36))
+        cpu = cpu_baseline(host_sample(synth, n_mats=7))
 
     if rank == 0:
         gbs = total_bytes * world / (ms * 1e-3) / 1e9
@@ -344,18 +373,21 @@ def main():
                 "vs_baseline": None, "dtype": "u8 codes x bf16 x, int32/fp32 accumulate", "data": "synthetic",
                 "tok_s_equiv": world * 1e3 / ms, "roofline_tok_s_equiv": peak * 1e9 / total_bytes,
                 "frac_of_hbm_peak": gbs / world / peak,
-                "config": {"workload": WORKLOAD, "weight_bytes_per_step": total_bytes,
-                           "launches_per_step": launches_per_step, "graph": "CUDA graph, programmatic dependent launch",
+                "config": {"workload": WORKLOAD, "weight_bytes_per_step": total_bytes, "variant": best,
+                           "launches_per_step": launches[best],
+                           "graph": "CUDA graph per step (launches: programmatic dependent launch)",
                            "l2": "inputs larger than L2 (2.49 GB of weights per step, read once)",
                            "parallelism": f"replicas x{world}"},
-                "roofline": {"bound": "hbm", "kernel": "gemv1_kernel<Q4_K> (all Q4_K products of a step)",
+                "variants": {k: {"ms_per_step": v, "GB/s": total_bytes * world / (v * 1e-3) / 1e9,
+                                 "launches_per_step": launches[k]} for k, v in variants.items()},
+                "roofline": {"bound": "hbm", "kernel": rf_kernel,
                              "achieved": achieved, "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs",
                              "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                             "launches": len(q4), "bytes_per_launch": q4_bytes / len(q4),
-                             "avg_launch_us": q4_ms * 1e3 / len(q4)},
+                             "launches": n_q4, "bytes_per_launch": q4_bytes / n_q4,
+                             "avg_launch_us": q4_ms * 1e3 / n_q4},
                 "e2e": {"value": total_bytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-                "gpu_launches": launches_per_step * args.steps,
+                "gpu_launches": launches[best] * args.steps,
                 "clocks": clk.summary()}
         if cpu is not None:
             line["cpu_baseline"] = cpu
