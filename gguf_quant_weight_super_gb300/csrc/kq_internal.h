@@ -57,6 +57,19 @@ cudaError_t prog_run(const ProgPlan* plan, void* ws, cudaStream_t stream);
 // L2 prefetch distance of the one-token kernel, in stages (0: none)
 void set_prefetch_stages(int pf);
 
+// Routed-expert products (kq_moe.cu).  Workspace: error word (offset 0),
+// plan, per-tile arrival counters, per-pair partial results.
+struct MoeLayout {
+  int Dmax;
+  int64_t ntiles;
+  size_t plan_off, cnt_off, part_off, bytes;
+};
+MoeLayout moe_layout(int64_t N, int64_t M, int top_k, int n_experts);
+bool moe_supported(int qtype, int64_t K, int64_t M, int top_k, int n_experts);
+cudaError_t launch_moe(int qtype, const void* W, int n_experts, const int32_t* ids, const float* gate,
+                       const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M, int top_k,
+                       void* ws, cudaStream_t st);
+
 cudaError_t launch_dequant(int qtype, const void* blocks, float* out, int64_t n_blocks, cudaStream_t stream);
 cudaError_t launch_unpack(int qtype, const void* blocks, int64_t n_blocks, uint8_t* codes, int8_t* scales,
                           uint8_t* mins, uint16_t* d_bits, uint16_t* dmin_bits, cudaStream_t stream);

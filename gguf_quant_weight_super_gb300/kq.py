@@ -31,6 +31,10 @@ SIGNATURES = {
     "kq_chain_workspace_size": (_SZ, [_P, _I]),
     "kq_chain_prepare": (_I, [_P, _I, _P, _SZ, _P, _P]),
     "kq_chain_run": (_I, [_P, _P, _P]),
+    "kq_moe_workspace_size": (_SZ, [_I64, _I64, ctypes.c_int32, ctypes.c_int32]),
+    "kq_moe_matvec": (_I, [_I, _P, ctypes.c_int32, _P, _P, _P, _I, _I, _P, _I64, _I64, _I64, ctypes.c_int32,
+                           _P, _SZ, _P]),
+    "kq_moe_check": (_I, [_P, _P]),
     "kq_device_error": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
     "kq_last_cuda_error": (_I, []),
     "kq_status_string": (ctypes.c_char_p, [_I]),
@@ -153,6 +157,29 @@ def kq_chain_prepare(ops, workspace, workspace_bytes, plan: KqChainPlan, stream=
 def kq_chain_run(plan: KqChainPlan, workspace, stream=None):
     _check("kq_chain_run", lib().kq_chain_run(ctypes.cast(ctypes.pointer(plan), ctypes.c_void_p), _ptr(workspace),
                                               _stream(stream)))
+
+
+def kq_moe_workspace_size(N, M, top_k, n_experts) -> int:
+    return lib().kq_moe_workspace_size(N, M, top_k, n_experts)
+
+
+def kq_moe_matvec(qtype, W_experts, n_experts, expert_ids, gate_w, x, x_dtype, x_per_slot, y, N, K, M, top_k,
+                  workspace, workspace_bytes, stream=None):
+    _check("kq_moe_matvec", lib().kq_moe_matvec(qtype, _ptr(W_experts), n_experts, _ptr(expert_ids), _ptr(gate_w),
+                                                _ptr(x), x_dtype, int(x_per_slot), _ptr(y), N, K, M, top_k,
+                                                _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def kq_moe_check(workspace, stream=None):
+    _check("kq_moe_check", lib().kq_moe_check(_ptr(workspace), _stream(stream)))
+
+
+def moe_workspace(N, M, top_k, n_experts, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace tensor for kq_moe_matvec (the caching allocator aligns it to 512 bytes)."""
+    n = kq_moe_workspace_size(N, M, top_k, n_experts)
+    if n == 0:
+        raise KQError("kq_moe_workspace_size", -4)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def kq_device_error(clear: bool = False) -> int:

@@ -71,7 +71,7 @@ typedef int kq_status;
 #define KQ_ERR_ARG (-1)         /* null pointer, negative size, bad dtype       */
 #define KQ_ERR_TYPE (-2)        /* unknown block type                           */
 #define KQ_ERR_SHAPE (-3)       /* K not a multiple of 32, n not a multiple of 256 */
-#define KQ_ERR_UNSUPPORTED (-4) /* M outside 1..16, top_k outside 1..32          */
+#define KQ_ERR_UNSUPPORTED (-4) /* a size outside the path's limits (M, top_k, K) */
 #define KQ_ERR_ALIGN (-5)       /* pointer alignment rule broken                 */
 #define KQ_ERR_CUDA (-6)        /* a CUDA call failed (see kq_last_cuda_error)   */
 #define KQ_ERR_WORKSPACE (-7)   /* workspace missing or too small                */
@@ -166,6 +166,54 @@ kq_status kq_chain_prepare(const kq_op *ops, int n_ops, void *workspace, size_t 
  * start, else KQ_ERR_CUDA.
  */
 kq_status kq_chain_run(const kq_chain_plan *plan, void *workspace, kq_stream_t stream);
+
+/*
+ * Routed-expert products (MoE decode and verify blocks).
+ *
+ * "GGUF in transformers", "Reusing ggml's Metal kernels": only the experts an
+ * MoE layer selected are read.  "ANE Fieldfare" README, "How it works": each
+ * token's router picks top_k of n_experts (8 of 128).
+ *
+ *   W_experts   n_experts matrices of N rows x ceil(K/256) blocks, back to
+ *               back: expert e starts at W_experts + e*N*ceil(K/256)*block_bytes
+ *   expert_ids  [M][top_k] int32
+ *   gate_w      [M][top_k] fp32, or NULL
+ *   x           [M][K] (x_per_slot = 0) or [M][top_k][K] (x_per_slot = 1)
+ *   y           gate_w != NULL: [M][N],  y[m] = sum_j gate_w[m][j] * W_{ids[m][j]} x_{m(,j)}
+ *               gate_w == NULL: [M][top_k][N], y[m][j] = W_{ids[m][j]} x_{m(,j)}
+ *
+ * The (token, slot) pairs are grouped by expert on the device, and every
+ * distinct routed expert's rows are read from memory once per call.  Sums
+ * are fp32 in a fixed order (the gate-weighted sum adds slots in order).
+ * An id outside [0, n_experts) never faults: its pair is dropped (no
+ * contribution; without gate_w its output row is not written) and the
+ * workspace's error word is set (kq_moe_check).
+ *
+ * workspace: kq_moe_workspace_size(N, M, top_k, n_experts) bytes of device
+ * memory, 256-byte aligned, zero-filled once before first use (arrival
+ * counters return to zero after every call); one call at a time per
+ * workspace.  After a call it holds the grouping, for inspection: at byte
+ * 256, int32 D (distinct experts), expert[Dmax] (ascending ids),
+ * offset[Dmax + 1], pair[M*top_k] (pair index m*top_k + j, grouped by expert,
+ * (m, j) order within an expert), Dmax = min(n_experts, M*top_k).
+ *
+ * Limits: M*top_k <= 512, n_experts <= 4096, K a multiple of 32, 32 rows of
+ * one expert at most 100 KB (K <= 5632 for Q4_K, 4608 for Q5_K, 3584 for
+ * Q6_K); else KQ_ERR_UNSUPPORTED.
+ */
+size_t kq_moe_workspace_size(int64_t N, int64_t M, int32_t top_k, int32_t n_experts);
+
+kq_status kq_moe_matvec(int type, const void *W_experts, int32_t n_experts, const int32_t *expert_ids,
+                        const float *gate_w, const void *x, int x_dtype, int x_per_slot, float *y, int64_t N,
+                        int64_t K, int64_t M, int32_t top_k, void *workspace, size_t workspace_bytes,
+                        kq_stream_t stream);
+
+/*
+ * Synchronize stream and read the workspace's error word: KQ_ERR_DEVICE if a
+ * routed id was out of range since the last check (the word is then
+ * cleared), else KQ_OK.
+ */
+kq_status kq_moe_check(void *workspace, kq_stream_t stream);
 
 /*
  * Read the device error word (KQ_OK when clean); with clear != 0 also reset

@@ -174,3 +174,18 @@ def moe_matvec(qtype: int, W_experts: np.ndarray, n_experts: int, ids: np.ndarra
     if rc != 0:
         raise ValueError(f"oracle_moe_matvec failed: {rc}")
     return y, s
+
+
+def moe_group(ids: np.ndarray, n_experts: int):
+    """Grouping of routed (token, slot) pairs by expert, by its definition:
+    the distinct valid ids in ascending order, and for each the pair indices
+    m*top_k + j holding it, in (m, j) order.  Ids outside [0, n_experts) are
+    left out.  Returns (experts, offsets, pairs) as Python lists."""
+    flat = [int(v) for v in np.asarray(ids).reshape(-1)]
+    experts = sorted({v for v in flat if 0 <= v < n_experts})
+    pairs, offsets = [], []
+    for e in experts:
+        offsets.append(len(pairs))
+        pairs.extend(i for i, v in enumerate(flat) if v == e)
+    offsets.append(len(pairs))
+    return experts, offsets, pairs

@@ -83,3 +83,26 @@ def test_chain_argument_errors_without_gpu(L):
         kq.kq_chain_prepare([ops(type=9)], 0x800000, 1 << 20, plan, stream=0)
     with pytest.raises(kq.KQError):                                      # workspace alignment
         kq.kq_chain_prepare([ops()], 0x800010, 1 << 20, plan, stream=0)
+
+
+def test_moe_argument_errors_without_gpu(L):
+    f = 0x100000
+    def call(**kw):
+        a = dict(type=1, W=f, E=128, ids=f, gate=None, x=f, xd=1, per_slot=0, y=0x200000, N=704, K=2816, M=1,
+                 top_k=8, ws=0x300000, wsb=1 << 24)
+        a.update(kw)
+        return L.kq_moe_matvec(a["type"], a["W"], a["E"], a["ids"], a["gate"], a["x"], a["xd"], a["per_slot"],
+                               a["y"], a["N"], a["K"], a["M"], a["top_k"], a["ws"], a["wsb"], None)
+    assert call(type=0) == -2
+    assert call(xd=3) == -1
+    assert call(K=700) == -3
+    assert call(M=0) == 0                                   # empty: no-op
+    assert call(top_k=0) == -1
+    assert call(M=100, top_k=8) == -4                       # more than 512 pairs
+    assert call(K=16384, type=3) == -4                      # 32 rows over the tile limit
+    assert call(W=0x100008) == -5
+    assert call(ws=None) == -7
+    assert call(ws=0x300010) == -7                          # workspace alignment
+    assert call(wsb=100) == -7
+    assert L.kq_moe_workspace_size(704, 1, 8, 128) > 0
+    assert L.kq_moe_workspace_size(704, 100, 8, 128) == 0

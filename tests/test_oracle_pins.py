@@ -300,3 +300,14 @@ def test_routing_generator_is_top_k_softmax():
     assert ids.shape == (16, 8) and gate.shape == (16, 8)
     assert all(len(set(r)) == 8 for r in ids)
     assert np.allclose(gate.sum(axis=1), 1.0, atol=1e-6) and np.all(np.diff(gate, axis=1) <= 0)
+
+
+def test_moe_group_by_definition():
+    import oracle
+    """Grouping pin: a hand-worked routing table (3 tokens, top-2, 5 experts,
+    one id out of range)."""
+    ids = np.array([[4, 1], [1, 0], [9, 4]], dtype=np.int32)
+    experts, offsets, pairs = oracle.moe_group(ids, 5)
+    assert experts == [0, 1, 4]
+    assert offsets == [0, 1, 3, 5]
+    assert pairs == [3, 1, 2, 0, 5]
