@@ -231,6 +231,137 @@ def run_single(args):
     print(json.dumps({"single": args.single, "runs": args.steps, "ok": True}))
 
 
+def _timed_graph(torch, fn, stream, steps, warmup):
+    g = capture(torch, fn, stream)
+    for _ in range(max(3, warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_workload(args):
+    """The other benchmark configurations, one JSON line each (measurements
+    behind the design notes; the default run is the dense sweep).  Inputs
+    smaller than L2 rotate through enough copies that every step reads HBM."""
+    import torch
+    from gguf_quant_weight_super_gb300 import build, kq, synth
+    build.build()
+    kq.lib()
+    dev = torch.device("cuda")
+    stream = torch.cuda.Stream()
+    peak, peak_kind = load_peaks()
+    L2_SPAN = 320 << 20  # bytes of distinct weights cycled through per replay
+
+    def bf16(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def line(name, nbytes, ms, extra):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out = {"workload": name, "metric": METRIC, "value": gbs, "unit": "GB/s", "ms_per_step": ms,
+               "weight_bytes_per_step": nbytes, "frac_of_hbm_peak": gbs / peak, "peak": peak,
+               "peak_kind": peak_kind, "tok_s_equiv": 1e3 / ms}
+        out.update(extra)
+        print(json.dumps(out), flush=True)
+
+    def dense(qt, N, K, M, xd, seed, label):
+        g = synth.rng(seed, qt, N, K)
+        W0 = synth.gen_matrix(qt, N, K, g)
+        ncopy = max(1, -(-L2_SPAN // W0.size))
+        Ws = [torch.from_numpy(W0).to(dev) for _ in range(ncopy)]
+        xn = synth.gen_x(M, K, g, xd)
+        x = bf16(xn) if xd == "bf16" else torch.from_numpy(xn).to(dev)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        xdt = kq.KQ_BF16 if xd == "bf16" else kq.KQ_F32
+
+        def step():
+            for W in Ws:
+                kq.kq_matvec(qt, W, x, xdt, y, N, K, M, stream)
+        ms = _timed_graph(torch, step, stream, args.steps, args.warmup) / ncopy
+        return W0.size, ms
+
+    wl = args.workload
+    if wl == "q4k_4096":
+        b, ms = dense(synth.Q4_K, 4096, 4096, 1, "f32", 0, "q4k")
+        line("single Q4_K 4096x4096, fp32 x, M=1", b, ms, {})
+    elif wl == "format_sweep":
+        res = {}
+        for qt, nm in ((synth.Q4_K, "Q4_K"), (synth.Q5_K, "Q5_K"), (synth.Q6_K, "Q6_K")):
+            for M in (1, 2, 4, 8):
+                b, ms = dense(qt, 4096, 14336, M, "bf16", 1, nm)
+                res[f"{nm}/M={M}"] = {"ms": ms, "GB/s": b / (ms * 1e-3) / 1e9, "bytes": b}
+        tot_b = sum(r["bytes"] for r in res.values())
+        tot_ms = sum(r["ms"] for r in res.values())
+        line("format sweep 4096x14336, Q4_K/Q5_K/Q6_K, M=1,2,4,8, bf16 x", tot_b, tot_ms, {"cases": res})
+    elif wl == "verify16":
+        res, tot_b, tot_ms = {}, 0, 0.0
+        for nm, N, K in (("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)):
+            b, ms = dense(synth.Q4_K, N, K, 16, "bf16", 3, nm)
+            res[nm] = {"ms": ms, "GB/s": b / (ms * 1e-3) / 1e9}
+            tot_b += b
+            tot_ms += ms
+        line("verify block M=16, gate/up 4096->14336, down 14336->4096, Q4_K, bf16 x", tot_b, tot_ms,
+             {"cases": res, "tok_s_equiv": 16e3 / tot_ms})
+    elif wl == "moe":
+        E, H, F, SH, top_k, layers = 128, 2816, 704, 2112, 8, 30
+        for M in (1, 16):
+            g = synth.rng(2, M)
+            Wg0 = synth.gen_matrix(synth.Q4_K, E * F, H, g)
+            Wd0 = synth.gen_matrix(synth.Q4_K, E * H, F, g)
+            per_layer = []
+            for li in range(layers):
+                gl = synth.rng(2, M, li)
+                ids, gate = synth.gen_routing(M, E, top_k, gl)
+                lay = {"Wg": torch.from_numpy(Wg0).to(dev), "Wu": torch.from_numpy(Wg0).to(dev),
+                       "Wd": torch.from_numpy(Wd0).to(dev), "ids": torch.from_numpy(ids).to(dev),
+                       "gate": torch.from_numpy(gate).to(dev), "nexp": len(set(ids.reshape(-1).tolist())),
+                       "Sg": torch.from_numpy(synth.gen_matrix(synth.Q4_K, SH, H, gl)).to(dev),
+                       "Su": torch.from_numpy(synth.gen_matrix(synth.Q4_K, SH, H, gl)).to(dev),
+                       "Sd": torch.from_numpy(synth.gen_matrix(synth.Q4_K, H, SH, gl)).to(dev)}
+                per_layer.append(lay)
+            x = bf16(synth.gen_x(M, H, g, "bf16"))
+            xs = bf16(synth.gen_x(M * top_k, F, g, "bf16"))
+            xsh = bf16(synth.gen_x(M, SH, g, "bf16"))
+            yg = torch.empty((M, top_k, F), dtype=torch.float32, device=dev)
+            yu = torch.empty_like(yg)
+            yd = torch.empty((M, H), dtype=torch.float32, device=dev)
+            ysh = torch.empty((M, SH), dtype=torch.float32, device=dev)
+            ysd = torch.empty((M, H), dtype=torch.float32, device=dev)
+            wsg = kq.moe_workspace(F, M, top_k, E)
+            wsd = kq.moe_workspace(H, M, top_k, E)
+
+            def step():
+                for L in per_layer:
+                    kq.kq_moe_matvec(synth.Q4_K, L["Wg"], E, L["ids"], None, x, kq.KQ_BF16, 0, yg, F, H, M, top_k,
+                                     wsg, wsg.numel(), stream)
+                    kq.kq_moe_matvec(synth.Q4_K, L["Wu"], E, L["ids"], None, x, kq.KQ_BF16, 0, yu, F, H, M, top_k,
+                                     wsg, wsg.numel(), stream)
+                    kq.kq_moe_matvec(synth.Q4_K, L["Wd"], E, L["ids"], L["gate"], xs, kq.KQ_BF16, 1, yd, H, F, M,
+                                     top_k, wsd, wsd.numel(), stream)
+                    kq.kq_matvec(synth.Q4_K, L["Sg"], x, kq.KQ_BF16, ysh, SH, H, M, stream)
+                    kq.kq_matvec(synth.Q4_K, L["Su"], x, kq.KQ_BF16, ysh, SH, H, M, stream)
+                    kq.kq_matvec(synth.Q4_K, L["Sd"], xsh, kq.KQ_BF16, ysd, H, SH, M, stream)
+            ms = _timed_graph(torch, step, stream, args.steps, args.warmup)
+            kq.kq_moe_check(wsg)
+            kq.kq_moe_check(wsd)
+            eb = synth.matrix_bytes(synth.Q4_K, F, H) * 2 + synth.matrix_bytes(synth.Q4_K, H, F)
+            sb = synth.matrix_bytes(synth.Q4_K, SH, H) * 2 + synth.matrix_bytes(synth.Q4_K, H, SH)
+            nbytes = sum(L["nexp"] * eb + sb for L in per_layer)
+            line(f"routed MoE decode, 30 layers, 128 experts top-8 + shared FFN, Q4_K, M={M}", nbytes, ms,
+                 {"tok_s_equiv": M * 1e3 / ms, "distinct_experts_per_layer": sum(L["nexp"] for L in per_layer) / layers,
+                  "launches_per_step": 6 * layers})
+            del per_layer
+            torch.cuda.empty_cache()
+    else:
+        raise SystemExit(f"unknown workload {wl}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -240,7 +371,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single", default=None,
                     help="profiling helper: run one product TYPE:NxK[:M] (e.g. Q4_K:19456x2560) --steps times")
+    ap.add_argument("--workload", default=None, choices=["q4k_4096", "format_sweep", "verify16", "moe"],
+                    help="time another configuration instead of the dense sweep (one JSON line each)")
     args = ap.parse_args()
+    if args.workload:
+        run_workload(args)
+        return
     if args.single:
         run_single(args)
         return

@@ -57,6 +57,11 @@ cudaError_t prog_run(const ProgPlan* plan, void* ws, cudaStream_t stream);
 // L2 prefetch distance of the one-token kernel, in stages (0: none)
 void set_prefetch_stages(int pf);
 
+// M = 2..16 tokens, bf16 x, on the tensor cores (kq_tc.cu)
+bool tc_supported(int qtype, int64_t N, int K, int M);
+cudaError_t launch_tc(int qtype, const void* W, const void* x, float* y, int64_t N, int K, int M,
+                      cudaStream_t stream, bool pdl);
+
 // Routed-expert products (kq_moe.cu).  Workspace: error word (offset 0),
 // plan, per-tile arrival counters, per-pair partial results.
 struct MoeLayout {

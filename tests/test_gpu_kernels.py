@@ -193,3 +193,21 @@ def test_full_format_sweep_4096x14336(qtype, M):
     rows = sorted(set(np.random.default_rng(M).integers(0, N, 256).tolist()) | {0, N - 1})
     y, yr, sr = _matvec_case(qtype, N, K, M, "bf16", 1, rows=rows)
     assert rel_err(y, yr, sr) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("N,K", [(14336, 4096), (4096, 14336)])
+def test_full_verify_block_m16(N, K):
+    """Speculative-verify block: M = 16 tokens against the gate/up and down
+    shapes (Q4_K, bf16 x) -- the tensor-core path; sampled rows."""
+    rows = sorted(set(np.random.default_rng(N).integers(0, N, 256).tolist()) | {0, N - 1})
+    y, yr, sr = _matvec_case(Q4_K, N, K, 16, "bf16", 3, rows=rows)
+    assert rel_err(y, yr, sr) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("NK", [(1, 256), (129, 704), (300, 2816), (128, 4096 + 96)])
+def test_matvec_m16_ragged(qtype, NK):
+    """Ragged row tiles (N not a multiple of 128) and K tails on the M = 16 path."""
+    N, K = NK
+    y, yr, sr = _matvec_case(qtype, N, K, 16, "bf16", 209)
+    assert rel_err(y, yr, sr) <= TOL["bf16"]
