@@ -226,6 +226,28 @@ kq_status kq_moe_matvec(int type, const void* W_experts, int32_t n_experts, cons
   return cuda_status(e);
 }
 
+kq_status kq_moe_matvec_noalloc(int type, const void* W_experts, int32_t n_experts, const int32_t* expert_ids,
+                                const float* gate_w, const void* x, int x_dtype, int x_per_slot, float* y, int64_t N,
+                                int64_t K, int64_t M, int32_t top_k, kq_stream_t stream) {
+  if (!valid_type(type)) return KQ_ERR_TYPE;
+  if (x_dtype != KQ_F32 && x_dtype != KQ_BF16) return KQ_ERR_ARG;
+  if (N < 0 || K < 0 || M < 0 || top_k <= 0 || n_experts <= 0) return KQ_ERR_ARG;
+  if (K % 32) return KQ_ERR_SHAPE;
+  if (N == 0 || M == 0) return KQ_OK;
+  if (K == 0 || !moe_supported(type, K, M, top_k, n_experts)) return KQ_ERR_UNSUPPORTED;
+  if (moe_layout(N, M, top_k, n_experts).bytes > moe_static_scratch_bytes()) return KQ_ERR_WORKSPACE;
+  if (!W_experts || !expert_ids || !x || !y) return KQ_ERR_ARG;
+  if (!aligned(W_experts, 16) || !aligned(x, 16) || !aligned(y, 4) || !aligned(expert_ids, 4) ||
+      (gate_w && !aligned(gate_w, 4)))
+    return KQ_ERR_ALIGN;
+  cudaError_t e = launch_moe_static(type, W_experts, n_experts, expert_ids, gate_w, x, x_dtype == KQ_BF16,
+                                    x_per_slot ? 1 : 0, y, N, static_cast<int>(K), static_cast<int>(M), top_k,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return KQ_ERR_UNSUPPORTED;
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_status(e);
+}
+
 kq_status kq_moe_check(void* workspace, kq_stream_t stream) {
   if (!workspace) return KQ_ERR_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

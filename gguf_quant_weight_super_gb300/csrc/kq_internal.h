@@ -74,6 +74,14 @@ bool moe_supported(int qtype, int64_t K, int64_t M, int top_k, int n_experts);
 cudaError_t launch_moe(int qtype, const void* W, int n_experts, const int32_t* ids, const float* gate,
                        const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M, int top_k,
                        void* ws, cudaStream_t st);
+cudaError_t launch_moe_err(int qtype, const void* W, int n_experts, const int32_t* ids, const float* gate,
+                           const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M, int top_k,
+                           void* ws, int* err, cudaStream_t st);
+// the same product with a library-owned static scratch array (no workspace)
+size_t moe_static_scratch_bytes();
+cudaError_t launch_moe_static(int qtype, const void* W, int n_experts, const int32_t* ids, const float* gate,
+                              const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M,
+                              int top_k, cudaStream_t st);
 
 cudaError_t launch_dequant(int qtype, const void* blocks, float* out, int64_t n_blocks, cudaStream_t stream);
 cudaError_t launch_unpack(int qtype, const void* blocks, int64_t n_blocks, uint8_t* codes, int8_t* scales,

@@ -278,9 +278,9 @@ bool moe_supported(int qtype, int64_t K, int64_t M, int top_k, int n_experts) {
          MT * row_bytes + 32 <= kMaxTileBytes;
 }
 
-cudaError_t launch_moe(int qtype, const void* W, int n_experts, const int32_t* ids, const float* gate,
-                       const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M, int top_k,
-                       void* ws, cudaStream_t st) {
+cudaError_t launch_moe_err(int qtype, const void* W, int n_experts, const int32_t* ids, const float* gate,
+                           const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M, int top_k,
+                           void* ws, int* err, cudaStream_t st) {
   const MoeLayout L = moe_layout(N, M, top_k, n_experts);
   uint8_t* w = static_cast<uint8_t*>(ws);
   MoeArgs a = {};
@@ -301,7 +301,7 @@ cudaError_t launch_moe(int qtype, const void* W, int n_experts, const int32_t* i
   a.gate = gate;
   a.x = x;
   a.y = y;
-  a.err = reinterpret_cast<int*>(w);
+  a.err = err;
   a.plan = reinterpret_cast<int*>(w + L.plan_off);
   a.cnt = reinterpret_cast<int*>(w + L.cnt_off);
   a.part = reinterpret_cast<float*>(w + L.part_off);
@@ -319,6 +319,47 @@ cudaError_t launch_moe(int qtype, const void* W, int n_experts, const int32_t* i
     case T_Q6_K * 4 + 3: return launch_moe_t<T_Q6_K, 3>(a, smem, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_moe(int qtype, const void* W, int n_experts, const int32_t* ids, const float* gate,
+                       const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M, int top_k,
+                       void* ws, cudaStream_t st) {
+  return launch_moe_err(qtype, W, n_experts, ids, gate, x, x_bf16, x_per_slot, y, N, K, M, top_k, ws,
+                        static_cast<int*>(ws), st);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the same kernel with its scratch in a file-scope
+// device array instead of a caller workspace.  For callers that cannot
+// allocate device memory at all -- a plain C host embedding libkq with no
+// device allocator of its own, or a decode loop that must not allocate -- and
+// so cannot provide the workspace kq_moe_matvec needs.  The array is zero at
+// module load; the arrival counters return to zero after every call; bad ids
+// are reported in the library's device error word (kq_device_error).  One
+// array per device: calls that overlap in time (any stream, any host thread)
+// race on it and must not be issued.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kMoeStaticScratch = 2u << 20;  // bytes: M*top_k*N <= ~500K outputs
+static __device__ __align__(256) uint8_t g_moe_scratch[kMoeStaticScratch];
+uint8_t* g_moe_scratch_ptr[64] = {nullptr};
+}  // namespace
+
+size_t moe_static_scratch_bytes() { return kMoeStaticScratch; }
+
+cudaError_t launch_moe_static(int qtype, const void* W, int n_experts, const int32_t* ids, const float* gate,
+                              const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M,
+                              int top_k, cudaStream_t st) {
+  if (moe_layout(N, M, top_k, n_experts).bytes > kMoeStaticScratch) return cudaErrorInvalidValue;
+  const int dev = current_device_id();
+  if (!g_moe_scratch_ptr[dev]) {  // once per device, with that device current
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_moe_scratch);
+    if (e != cudaSuccess) return e;
+    g_moe_scratch_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  return launch_moe_err(qtype, W, n_experts, ids, gate, x, x_bf16, x_per_slot, y, N, K, M, top_k,
+                        g_moe_scratch_ptr[dev], device_error_ptr(), st);
 }
 
 }  // namespace kq

@@ -35,6 +35,8 @@ SIGNATURES = {
     "kq_moe_matvec": (_I, [_I, _P, ctypes.c_int32, _P, _P, _P, _I, _I, _P, _I64, _I64, _I64, ctypes.c_int32,
                            _P, _SZ, _P]),
     "kq_moe_check": (_I, [_P, _P]),
+    "kq_moe_matvec_noalloc": (_I, [_I, _P, ctypes.c_int32, _P, _P, _P, _I, _I, _P, _I64, _I64, _I64,
+                                   ctypes.c_int32, _P]),
     "kq_device_error": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
     "kq_last_cuda_error": (_I, []),
     "kq_status_string": (ctypes.c_char_p, [_I]),
@@ -168,6 +170,13 @@ def kq_moe_matvec(qtype, W_experts, n_experts, expert_ids, gate_w, x, x_dtype, x
     _check("kq_moe_matvec", lib().kq_moe_matvec(qtype, _ptr(W_experts), n_experts, _ptr(expert_ids), _ptr(gate_w),
                                                 _ptr(x), x_dtype, int(x_per_slot), _ptr(y), N, K, M, top_k,
                                                 _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def kq_moe_matvec_noalloc(qtype, W_experts, n_experts, expert_ids, gate_w, x, x_dtype, x_per_slot, y, N, K, M,
+                          top_k, stream=None):
+    _check("kq_moe_matvec_noalloc",
+           lib().kq_moe_matvec_noalloc(qtype, _ptr(W_experts), n_experts, _ptr(expert_ids), _ptr(gate_w), _ptr(x),
+                                       x_dtype, int(x_per_slot), _ptr(y), N, K, M, top_k, _stream(stream)))
 
 
 def kq_moe_check(workspace, stream=None):

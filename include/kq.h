@@ -209,6 +209,27 @@ kq_status kq_moe_matvec(int type, const void *W_experts, int32_t n_experts, cons
                         kq_stream_t stream);
 
 /*
+ * kq_moe_matvec without a workspace: the same product, with its scratch in a
+ * fixed 2 MiB array inside libkq (one per device).  The pages have no
+ * counterpart of this call: it exists for callers that cannot allocate
+ * device memory (a C host with no device allocator, or a decode loop that
+ * must not allocate), which therefore cannot pass the workspace above.
+ *   - Limit: the call returns KQ_ERR_WORKSPACE when the workspace
+ *     kq_moe_workspace_size(N, M, top_k, n_experts) would exceed 2 MiB.
+ *   - It allocates nothing.  The first call on each device looks up the
+ *     array's address once (cudaGetSymbolAddress); make that first call
+ *     before any stream capture begins.
+ *   - The array is zero when the library loads and is left with its arrival
+ *     counters at zero after every call; a routed id out of range is reported
+ *     in the library's device error word (kq_device_error), not in a workspace.
+ *   - Calls that overlap in time (on any stream or host thread) share the
+ *     array and race: issue them one after another.
+ */
+kq_status kq_moe_matvec_noalloc(int type, const void *W_experts, int32_t n_experts, const int32_t *expert_ids,
+                                const float *gate_w, const void *x, int x_dtype, int x_per_slot, float *y,
+                                int64_t N, int64_t K, int64_t M, int32_t top_k, kq_stream_t stream);
+
+/*
  * Synchronize stream and read the workspace's error word: KQ_ERR_DEVICE if a
  * routed id was out of range since the last check (the word is then
  * cleared), else KQ_OK.
