@@ -220,12 +220,14 @@ def run_single(args):
     qt = {"Q4_K": synth.Q4_K, "Q5_K": synth.Q5_K, "Q6_K": synth.Q6_K}[spec[0]]
     N, K = (int(v) for v in spec[1].split("x"))
     M = int(spec[2]) if len(spec) > 2 else 1
+    xd = spec[3] if len(spec) > 3 else "bf16"
     g = synth.rng(0, qt, N, K)
     W = torch.from_numpy(synth.gen_matrix(qt, N, K, g)).cuda()
-    x = torch.from_numpy(synth.gen_x(M, K, g, "bf16").view(np.int16)).cuda().view(torch.bfloat16)
+    xn = synth.gen_x(M, K, g, xd)
+    x = torch.from_numpy(xn.view(np.int16)).cuda().view(torch.bfloat16) if xd == "bf16" else torch.from_numpy(xn).cuda()
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
     for _ in range(args.steps):
-        kq.kq_matvec(qt, W, x, kq.KQ_BF16, y, N, K, M)
+        kq.kq_matvec(qt, W, x, kq.KQ_BF16 if xd == "bf16" else kq.KQ_F32, y, N, K, M)
     torch.cuda.synchronize()
     assert kq.kq_device_error() == 0
     print(json.dumps({"single": args.single, "runs": args.steps, "ok": True}))
@@ -370,7 +372,7 @@ def main():
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single", default=None,
-                    help="profiling helper: run one product TYPE:NxK[:M] (e.g. Q4_K:19456x2560) --steps times")
+                    help="profiling helper: run one product TYPE:NxK[:M[:f32|bf16]] (e.g. Q4_K:19456x2560) --steps times")
     ap.add_argument("--workload", default=None, choices=["q4k_4096", "format_sweep", "verify16", "moe"],
                     help="time another configuration instead of the dense sweep (one JSON line each)")
     args = ap.parse_args()

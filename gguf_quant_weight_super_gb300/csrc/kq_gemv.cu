@@ -345,7 +345,10 @@ __device__ __forceinline__ void prefetch_stage(const StageCursor& c, int lane) {
 // buffers, the x image.
 __host__ __device__ inline size_t red_bytes(int S) { return static_cast<size_t>(S + 1) * NC * TT * 4; }
 
-template <bool PROG>
+// PROG: ops in global memory (any types); else the single op a.op0, whose
+// type and x limb count are the template's QT0 and NL0 (one instantiation per
+// format and x dtype keeps the single-product code small).
+template <bool PROG, int QT0, int NL0>
 __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ ProgArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   Ring rg;
@@ -431,6 +434,13 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
       }
     }
     const XImg xi = ximg_at(xbase, a.nb_max, a.nl_max);
+    if constexpr (!PROG) {
+      consumer_sync();
+      stage_x<NL0, NTHC>(o.x, NL0 == 2, o.K, o.nb, xi, ctid);
+      consumer_sync();
+      consume_op<QT0, NL0>(o, xi, rg, rd, wk, a.err, cta, G);
+      continue;
+    }
     if (oi == 0 || (o.flags & (OP_NEWX | OP_WAIT))) {
       consumer_sync();  // every consumer is done with the previous x image
       if (NL == 2) stage_x<2, NTHC>(o.x, 1, o.K, o.nb, xi, ctid);
@@ -537,14 +547,14 @@ bool ring_geom(int64_t max_stage, int nb_max, int nl_max, LaunchGeom& g) {
   return true;
 }
 
-template <bool PROG>
+template <bool PROG, int QT0, int NL0>
 cudaError_t launch_prog(ProgArgs& a, const LaunchGeom& g, bool cooperative, cudaStream_t st, bool pdl) {
   a.S = g.S;
   a.slot = g.slot;
   static bool smem_set[64] = {false};
   const int dev = current_device_id();
   if (!smem_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prog_kernel<PROG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prog_kernel<PROG, QT0, NL0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kMaxSmemPerBlock);
     if (e != cudaSuccess) return e;
     smem_set[dev] = true;
@@ -568,7 +578,7 @@ cudaError_t launch_prog(ProgArgs& a, const LaunchGeom& g, bool cooperative, cuda
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, prog_kernel<PROG>, a);
+  return cudaLaunchKernelEx(&cfg, prog_kernel<PROG, QT0, NL0>, a);
 }
 
 // Program workspace: header (grid barrier counter), ops, split-K partials and counters.
@@ -606,7 +616,15 @@ cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, 
   a.barrier = nullptr;
   a.err = device_error_ptr();
   a.pf = g_prefetch_stages;
-  return launch_prog<false>(a, g, false, stream, pdl);
+  switch (qtype * 4 + (x_bf16 ? 2 : 3)) {
+    case T_Q4_K * 4 + 2: return launch_prog<false, T_Q4_K, 2>(a, g, false, stream, pdl);
+    case T_Q4_K * 4 + 3: return launch_prog<false, T_Q4_K, 3>(a, g, false, stream, pdl);
+    case T_Q5_K * 4 + 2: return launch_prog<false, T_Q5_K, 2>(a, g, false, stream, pdl);
+    case T_Q5_K * 4 + 3: return launch_prog<false, T_Q5_K, 3>(a, g, false, stream, pdl);
+    case T_Q6_K * 4 + 2: return launch_prog<false, T_Q6_K, 2>(a, g, false, stream, pdl);
+    case T_Q6_K * 4 + 3: return launch_prog<false, T_Q6_K, 3>(a, g, false, stream, pdl);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // Plans the whole program on the host and returns the workspace bytes it
@@ -723,7 +741,7 @@ cudaError_t prog_run(const ProgPlan* plan, void* ws, cudaStream_t stream) {
   g.slot = plan->slot;
   g.smem = static_cast<size_t>(plan->smem);
   // grid barriers need every CTA resident: cooperative launch
-  return launch_prog<true>(a, g, plan->coop != 0, stream, plan->coop == 0);
+  return launch_prog<true, 0, 0>(a, g, plan->coop != 0, stream, plan->coop == 0);
 }
 
 }  // namespace kq

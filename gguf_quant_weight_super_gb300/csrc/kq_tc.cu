@@ -195,7 +195,8 @@ __device__ __forceinline__ void load_b(const TcArgs& a, int blk, int t128, uint4
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int u = t128 + 128 * i;
-    const int n = u >> 5, kc = u & 31;  // token, 8-value chunk within the block
+    const int n = u & 15, kc = u >> 4;  // token, 8-value chunk within the block (tokens vary fastest:
+                                        // 8 neighbouring threads store 8 consecutive 16-byte rows)
     const int k = 256 * blk + 8 * kc;
     v[i] = make_uint4(0, 0, 0, 0);
     if (n < a.M && k < a.K) v[i] = *reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(n) * a.K + k);
@@ -206,7 +207,7 @@ __device__ __forceinline__ void store_b(int t128, const uint4 (&v)[4], uint8_t* 
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int u = t128 + 128 * i;
-    const int n = u >> 5, kc = u & 31;
+    const int n = u & 15, kc = u >> 4;
     *reinterpret_cast<uint4*>(bstage + kc * 128 + (n >> 3) * 4096 + (n & 7) * 16) = v[i];
   }
 }
