@@ -5,12 +5,15 @@ decoder (hidden 2560; q 2560->4096, k/v 2560->1024, o 4096->2560, gate/up
 2560->9728, down 9728->2560; LM head 2560->151936), Q4_K everywhere except
 Q6_K for v_proj and down_proj on even layers and for the LM head, in decode
 order (q, k, v share an input; gate, up share an input; each stage waits for
-the previous one).  Two ways to run the step through libkq are timed:
-  launches: one kq_matvec per matrix (253), captured in a CUDA graph whose
-            kernels are chained with programmatic dependent launch;
-  chain:    one kq_chain_run of the 253 products, a grid barrier before every
-            stage (one persistent launch per step).
-The headline value is the faster of the two; both are reported.
+the previous one).  Three ways to run the step through libkq are timed, each
+captured in a CUDA graph whose kernels are chained with programmatic
+dependent launch:
+  launches: one kq_matvec per matrix (253 launches);
+  stages:   one launch per stage -- a barrier-free kq_chain_run for q|k|v and
+            gate|up, kq_matvec for o, down and the head (145 launches);
+  chain:    one kq_chain_run of all 253 products with a grid barrier before
+            every stage (one persistent launch per step).
+The headline value is the fastest; all are reported.
 
 Prints one JSON line.  `value` is quantized-weight GB/s (stored weight bytes
 read per second); tok/s-equivalent = steps per second.  Inputs are synthetic
@@ -408,9 +411,21 @@ def main():
     stream = torch.cuda.Stream()
 
     chain = make_chain(kq, mats, xs)
+    # the independent products of a stage (q|k|v, gate|up) as one launch each
+    stage_runs = []
+    for si in range(len(stages)):
+        sm = [m for m in mats if m["stage"] == si]
+        if len(sm) == 1:
+            m = sm[0]
+            stage_runs.append(lambda m=m: kq.kq_matvec(m["type"], m["W"], xs[m["stage"]], kq.KQ_BF16, m["y"], m["N"],
+                                                        m["K"], 1, stream))
+        else:
+            ch = make_chain(kq, sm, xs)
+            stage_runs.append(lambda ch=ch: ch.run(stream))
     graphs = {"launches": capture(torch, lambda: record_step(kq, torch, mats, xs, stream), stream),
+              "stages": capture(torch, lambda: [r() for r in stage_runs], stream),
               "chain": capture(torch, lambda: chain.run(stream), stream)}
-    launches = {"launches": launches_per_step, "chain": 1}
+    launches = {"launches": launches_per_step, "stages": len(stage_runs), "chain": 1}
 
     def barrier():
         if dist is not None:
@@ -449,9 +464,10 @@ def main():
     # step; for separate launches, the Q4_K products of a step timed alone
     # (same order, same chaining).
     peak, peak_kind = load_peaks()
-    if best == "chain":
-        q4_bytes, n_q4, q4_ms = total_bytes, 1, ms
-        rf_kernel = "prog_kernel (chain: all 253 products of a step, one launch)"
+    if best in ("chain", "stages"):
+        q4_bytes, n_q4, q4_ms = total_bytes, launches[best], ms
+        rf_kernel = ("prog_kernel (chain: all 253 products of a step, one launch)" if best == "chain" else
+                     "prog_kernel (one launch per stage: q|k|v, o, gate|up, down; 145 per step)")
     else:
         q4 = [m for m in mats if m["type"] == synth.Q4_K]
         q4_bytes, n_q4 = sum(m["bytes"] for m in q4), len(q4)

@@ -644,8 +644,12 @@ bool split_allowed(const ProgOpDesc* d, int n_ops, int i) {
 }
 
 // Plan every op of a program; false if some op cannot run on this path.
+// K is split only in programs with grid barriers (a program without them is
+// an ordinary launch that overlaps its neighbours and needs no final barrier).
 bool plan_prog(const ProgOpDesc* descs, int n_ops, KqOp* ops, size_t* part_bytes) {
   const int G = num_sms();
+  bool any_wait = false;
+  for (int i = 1; i < n_ops; ++i) any_wait = any_wait || descs[i].wait_previous;
   size_t pb = 0;
   for (int i = 0; i < n_ops; ++i) {
     KqOp o = {};
@@ -656,7 +660,7 @@ bool plan_prog(const ProgOpDesc* descs, int n_ops, KqOp* ops, size_t* part_bytes
     o.K = static_cast<int32_t>(descs[i].K);
     o.type = descs[i].type;
     o.x_bf16 = descs[i].x_bf16;
-    if (!plan_op(o, G, split_allowed(descs, n_ops, i), kSlotCap)) return false;
+    if (!plan_op(o, G, any_wait && split_allowed(descs, n_ops, i), kSlotCap)) return false;
     if (o.KS > 1) pb += align256(static_cast<size_t>(o.ntiles) * o.KS * TT * sizeof(float));
     ops[i] = o;
   }

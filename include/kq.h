@@ -161,9 +161,11 @@ kq_status kq_chain_prepare(const kq_op *ops, int n_ops, void *workspace, size_t 
                            kq_chain_plan *plan, kq_stream_t stream);
 
 /*
- * Run a prepared chain on stream.  A chain with wait_previous ops (or with
- * split-K outputs) is a cooperative launch: one CTA per SM must be able to
- * start, else KQ_ERR_CUDA.
+ * Run a prepared chain on stream.  A chain with wait_previous ops is a
+ * cooperative launch (one CTA per SM must be able to start, else
+ * KQ_ERR_CUDA).  A chain without them (independent products sharing one
+ * launch, e.g. q|k|v) is an ordinary launch with programmatic stream
+ * serialization, like kq_matvec.
  */
 kq_status kq_chain_run(const kq_chain_plan *plan, void *workspace, kq_stream_t stream);
 
