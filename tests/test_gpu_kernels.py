@@ -211,3 +211,24 @@ def test_matvec_m16_ragged(qtype, NK):
     N, K = NK
     y, yr, sr = _matvec_case(qtype, N, K, 16, "bf16", 209)
     assert rel_err(y, yr, sr) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("xd", ["f32", "bf16"])
+def test_matvec_x_extreme_runs(qtype, xd):
+    """Runs of x whose maximum is subnormal, tiny, huge or zero take the
+    block-float staging's slow path; every product must still match."""
+    N, K = 70, 1536
+    g = synth.rng(210, qtype)
+    W = synth.gen_matrix(qtype, N, K, g)
+    x = g.standard_normal((1, K)).astype(np.float32)
+    x[0, 0:128] *= 1e-39      # subnormal run
+    x[0, 128:256] *= 1e-30    # tiny normal run
+    x[0, 256:384] *= 1e30     # huge run
+    x[0, 384:512] = 0.0       # zero run
+    x[0, 512:640] *= 1e-20
+    if xd == "bf16":
+        x = synth.to_bf16_bits(x)
+    y = kq.matvec(qtype, dev(W), x_dev(x), N, K).cpu().numpy()
+    yr, sr = oracle.matvec(qtype, W, N, K, x, threads=8)
+    assert rel_err(y, yr, sr) <= TOL[xd]
