@@ -73,7 +73,8 @@ struct KqOp {
   const void* x;
   float* y;
   float* part;       // split K: partial row sums [KS][ntiles*TT] (workspace), else null
-  int64_t pad0;
+  int32_t R;         // rows per quad: a tile is 8R rows (programs: R = 4)
+  int32_t pad0;
   int64_t N;
   int64_t row_bytes;
   int32_t K, nb, type, x_bf16;
@@ -115,10 +116,10 @@ __device__ __forceinline__ int first_unit(const KqOp& o, int cta, int G) {
 // into slot + i*srb, as its 16-byte aligned superset; arrive on full.
 __device__ __forceinline__ void produce(const KqOp& o, int tile, int b0, int n, uint8_t* slot, uint64_t* full,
                                        int lane, int BB) {
-  const int64_t r0 = static_cast<int64_t>(tile) * TT;
+  const int64_t r0 = static_cast<int64_t>(tile) * (8 * o.R);
   uint32_t len = 0;
   const uint8_t* src = nullptr;
-  if (r0 + lane < o.N) {
+  if (lane < 8 * o.R && r0 + lane < o.N) {
     const uintptr_t s0 =
         reinterpret_cast<uintptr_t>(o.W + (r0 + lane) * o.row_bytes + static_cast<int64_t>(b0) * BB);
     const uintptr_t e0 = s0 + static_cast<uintptr_t>(n) * BB;
@@ -167,10 +168,10 @@ struct Walk {
 };
 
 // Consumers: every unit of op o for this CTA.  Quad q of every warp owns the
-// tile rows q, q+8, q+16, q+24; the stage's blocks are dealt to the warps
-// round-robin (continuing across stages), so a warp applies one x slice to
-// the 4 rows of each of its 8 quads.
-template <int QT, int NL>
+// tile rows q, q+8, ... (R of them; a tile is 8R rows); the stage's blocks
+// are dealt to the warps round-robin (continuing across stages), so a warp
+// applies one x slice to the R rows of each of its 8 quads.
+template <int QT, int NL, int R>
 __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const Red& rd, Walk& wk, int* err,
                            int cta, int G) {
   constexpr int BB = Fmt<QT>::BYTES;
@@ -182,8 +183,10 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
     const int tile = u / o.KS, kp = u - tile * o.KS;
     const int kb0 = kp * o.kpb;
     const int kb1 = min(o.nb, kb0 + o.kpb);
-    const int64_t row0 = static_cast<int64_t>(tile) * TT;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const int64_t row0 = static_cast<int64_t>(tile) * (8 * R);
+    float acc[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) acc[i] = 0.0f;
     for (int b0 = kb0; b0 < kb1; b0 += o.KC) {
       const int n = min(o.KC, kb1 - b0);
       const int slot = static_cast<int>(wk.q % rg.S);
@@ -198,9 +201,9 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
         // stale shared memory and never written)
         const uint32_t sp = rg.base_s + static_cast<uint32_t>(slot) * rg.slot;
         const uint32_t seg0 = static_cast<uint32_t>(row0 * o.row_bytes) + static_cast<uint32_t>(b0 * BB);
-        uint32_t rp[4];
+        uint32_t rp[R];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < R; ++i) {
           const int r = quad + 8 * i;
           // W is 16-byte aligned: the segment's offset in its 16-byte granule
           const uint32_t off = (seg0 + static_cast<uint32_t>(r) * static_cast<uint32_t>(o.row_bytes)) & 15u;
@@ -216,15 +219,15 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
             const int4 si = make_int4(static_cast<int>(sv.x), static_cast<int>(sv.y), static_cast<int>(sv.z),
                                       static_cast<int>(sv.w));
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = core_q6<NL>(rp[i], X, si, s, c, acc[i]);
+            for (int i = 0; i < R; ++i) acc[i] = core_q6<NL>(rp[i], X, si, s, c, acc[i]);
           } else {
             const uint2 sv = lds64(xi.si32_s + 4 * (8 * b + 2 * c));
             const int2 si = make_int2(static_cast<int>(sv.x), static_cast<int>(sv.y));
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = core_q45<QT, NL>(rp[i], X, si, s, c, sl, acc[i]);
+            for (int i = 0; i < R; ++i) acc[i] = core_q45<QT, NL>(rp[i], X, si, s, c, sl, acc[i]);
           }
 #pragma unroll
-          for (int i = 0; i < 4; ++i) rp[i] += NC * BB;
+          for (int i = 0; i < R; ++i) rp[i] += NC * BB;
         }
       }
       wk.cb = (wk.cb + n) % NC;
@@ -234,7 +237,7 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
     }
     // this warp's partial row sums: over the quad's lanes, then to shared memory
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < R; ++i) {
       acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xFFFFFFFFu, acc[i], 1));
       acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xFFFFFFFFu, acc[i], 2));
     }
@@ -243,7 +246,7 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
     float* rb = rd.buf + static_cast<size_t>(rs) * NC * TT;
     if (c == 0) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) rb[warp * TT + quad + 8 * i] = acc[i];
+      for (int i = 0; i < R; ++i) rb[warp * TT + quad + 8 * i] = acc[i];
     }
     __syncwarp();
     int last = 0;
@@ -261,7 +264,7 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
     __syncwarp();
     if (lane == 0) rd.cnt[rs] = 0;
     const int64_t row = row0 + lane;
-    if (row < o.N && !wk.failed) {
+    if (lane < 8 * R && row < o.N && !wk.failed) {
       if (o.KS == 1) o.y[row] = v;
       else o.part[static_cast<int64_t>(kp) * o.ntiles * TT + row] = v;  // added at the next grid barrier
     }
@@ -282,9 +285,9 @@ __device__ __forceinline__ void fixup_op(const KqOp& o, int cta, int G, int ctid
 template <int NL>
 __device__ __forceinline__ void consume_any(const KqOp& o, const XImg& xi, const Ring& rg, const Red& rd, Walk& wk,
                                             int* err, int cta, int G) {
-  if (o.type == T_Q4_K) consume_op<T_Q4_K, NL>(o, xi, rg, rd, wk, err, cta, G);
-  else if (o.type == T_Q5_K) consume_op<T_Q5_K, NL>(o, xi, rg, rd, wk, err, cta, G);
-  else consume_op<T_Q6_K, NL>(o, xi, rg, rd, wk, err, cta, G);
+  if (o.type == T_Q4_K) consume_op<T_Q4_K, NL, 4>(o, xi, rg, rd, wk, err, cta, G);
+  else if (o.type == T_Q5_K) consume_op<T_Q5_K, NL, 4>(o, xi, rg, rd, wk, err, cta, G);
+  else consume_op<T_Q6_K, NL, 4>(o, xi, rg, rd, wk, err, cta, G);
 }
 
 template <bool PROG>
@@ -332,8 +335,8 @@ __device__ __forceinline__ void cur_next(const ProgArgs& a, StageCursor& c, int 
 __device__ __forceinline__ void prefetch_stage(const StageCursor& c, int lane) {
   const int BB = block_bytes_of(c.o.type);
   const int n = min(c.o.KC, c.kb1 - c.b0);
-  const int64_t row = static_cast<int64_t>(c.tile) * TT + lane;
-  if (row < c.o.N) {
+  const int64_t row = static_cast<int64_t>(c.tile) * (8 * c.o.R) + lane;
+  if (lane < 8 * c.o.R && row < c.o.N) {
     const uintptr_t s0 = reinterpret_cast<uintptr_t>(c.o.W + row * c.o.row_bytes + static_cast<int64_t>(c.b0) * BB);
     const uintptr_t e0 = s0 + static_cast<uintptr_t>(n) * BB;
     const uintptr_t as = s0 & ~uintptr_t(15), ae = (e0 + 15) & ~uintptr_t(15);
@@ -348,7 +351,7 @@ __host__ __device__ inline size_t red_bytes(int S) { return static_cast<size_t>(
 // PROG: ops in global memory (any types); else the single op a.op0, whose
 // type and x limb count are the template's QT0 and NL0 (one instantiation per
 // format and x dtype keeps the single-product code small).
-template <bool PROG, int QT0, int NL0>
+template <bool PROG, int QT0, int NL0, int R0>
 __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ ProgArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   Ring rg;
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
       consumer_sync();
       stage_x<NL0, NTHC>(o.x, NL0 == 2, o.K, o.nb, xi, ctid);
       consumer_sync();
-      consume_op<QT0, NL0>(o, xi, rg, rd, wk, a.err, cta, G);
+      consume_op<QT0, NL0, R0>(o, xi, rg, rd, wk, a.err, cta, G);
       continue;
     }
     if (oi == 0 || (o.flags & (OP_NEWX | OP_WAIT))) {
@@ -497,17 +500,29 @@ int seg_stride(int type, int kc) {
 // Geometry of one op: K-parts KS (only with a workspace) and stage width KC.
 // cost = block-chunks of the busiest CTA (a chunk = one block for 32 rows,
 // dealt to one warp), plus a fixed cost per stage and per split.
-bool plan_op(KqOp& o, int G, bool allow_split, int64_t slot_cap) {
+bool plan_op(KqOp& o, int G, bool allow_split, int64_t slot_cap, bool allow_short_tiles = false) {
   const int BB = block_bytes_of(o.type);
   if (!BB || o.K <= 0 || o.K % 32 || o.N <= 0) return false;
   o.nb = (o.K + 255) / 256;
   if (o.nb > MAX_NB) return false;
   o.row_bytes = static_cast<int64_t>(o.nb) * BB;
-  const int64_t ntiles = (o.N + TT - 1) / TT;
+  // tile height 8R: the busiest CTA's rows, rounds * 8R, with shorter tiles
+  // charged for their lost x reuse (one x slice serves R rows)
+  o.R = 4;
+  if (allow_short_tiles) {
+    double best = -1.0;
+    for (int r : {4, 2, 1}) {
+      const int64_t nt = (o.N + 8 * r - 1) / (8 * r);
+      const double cost = static_cast<double>((nt + G - 1) / G) * 8 * r * (1.0 + 0.08 * (4 / r - 1));
+      if (best < 0 || cost < best - 1e-9) { best = cost; o.R = r; }
+    }
+  }
+  const int TTo = 8 * o.R;
+  const int64_t ntiles = (o.N + TTo - 1) / TTo;
   if (ntiles > (int64_t(1) << 28)) return false;
   int kcmax = o.nb;
-  while (kcmax > 1 && static_cast<int64_t>(TT) * seg_stride(o.type, kcmax) > slot_cap) --kcmax;
-  if (static_cast<int64_t>(TT) * seg_stride(o.type, kcmax) > slot_cap) return false;
+  while (kcmax > 1 && static_cast<int64_t>(TTo) * seg_stride(o.type, kcmax) > slot_cap) --kcmax;
+  if (static_cast<int64_t>(TTo) * seg_stride(o.type, kcmax) > slot_cap) return false;
   // K-parts (with a workspace): minimise the busiest CTA's blocks,
   // ceil(tiles*KS / G) * ceil(nb / KS), plus one block per split level
   int KS = 1;
@@ -529,7 +544,7 @@ bool plan_op(KqOp& o, int G, bool allow_split, int64_t slot_cap) {
   return true;
 }
 
-int64_t stage_bytes(const KqOp& o) { return static_cast<int64_t>(TT) * o.srb; }
+int64_t stage_bytes(const KqOp& o) { return static_cast<int64_t>(8 * o.R) * o.srb; }
 
 struct LaunchGeom {
   int S, slot;
@@ -547,14 +562,14 @@ bool ring_geom(int64_t max_stage, int nb_max, int nl_max, LaunchGeom& g) {
   return true;
 }
 
-template <bool PROG, int QT0, int NL0>
+template <bool PROG, int QT0, int NL0, int R0>
 cudaError_t launch_prog(ProgArgs& a, const LaunchGeom& g, bool cooperative, cudaStream_t st, bool pdl) {
   a.S = g.S;
   a.slot = g.slot;
   static bool smem_set[64] = {false};
   const int dev = current_device_id();
   if (!smem_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prog_kernel<PROG, QT0, NL0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prog_kernel<PROG, QT0, NL0, R0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kMaxSmemPerBlock);
     if (e != cudaSuccess) return e;
     smem_set[dev] = true;
@@ -578,7 +593,7 @@ cudaError_t launch_prog(ProgArgs& a, const LaunchGeom& g, bool cooperative, cuda
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, prog_kernel<PROG, QT0, NL0>, a);
+  return cudaLaunchKernelEx(&cfg, prog_kernel<PROG, QT0, NL0, R0>, a);
 }
 
 // Program workspace: header (grid barrier counter), ops, split-K partials and counters.
@@ -590,6 +605,28 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 namespace {
 int g_prefetch_stages = 8;  // L2 prefetch distance (stages beyond the one being copied)
+
+template <int QT, int NL>
+cudaError_t launch_single_r(int R, ProgArgs& a, const LaunchGeom& g, cudaStream_t st, bool pdl) {
+  switch (R) {
+    case 4: return launch_prog<false, QT, NL, 4>(a, g, false, st, pdl);
+    case 2: return launch_prog<false, QT, NL, 2>(a, g, false, st, pdl);
+    case 1: return launch_prog<false, QT, NL, 1>(a, g, false, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+// One instantiation per (format, x limbs, rows per quad).
+cudaError_t launch_single(int qtype, int NL, int R, ProgArgs& a, const LaunchGeom& g, cudaStream_t st, bool pdl) {
+  switch (qtype * 4 + NL) {
+    case T_Q4_K * 4 + 2: return launch_single_r<T_Q4_K, 2>(R, a, g, st, pdl);
+    case T_Q4_K * 4 + 3: return launch_single_r<T_Q4_K, 3>(R, a, g, st, pdl);
+    case T_Q5_K * 4 + 2: return launch_single_r<T_Q5_K, 2>(R, a, g, st, pdl);
+    case T_Q5_K * 4 + 3: return launch_single_r<T_Q5_K, 3>(R, a, g, st, pdl);
+    case T_Q6_K * 4 + 2: return launch_single_r<T_Q6_K, 2>(R, a, g, st, pdl);
+    case T_Q6_K * 4 + 3: return launch_single_r<T_Q6_K, 3>(R, a, g, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
 }  // namespace
 void set_prefetch_stages(int pf) { g_prefetch_stages = pf < 0 ? 0 : pf; }
 
@@ -606,7 +643,7 @@ cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, 
   o.type = qtype;
   o.x_bf16 = x_bf16;
   o.flags = OP_NEWX;
-  if (!plan_op(o, num_sms(), false, kSlotCap)) return cudaErrorNotSupported;
+  if (!plan_op(o, num_sms(), false, kSlotCap, true)) return cudaErrorNotSupported;
   LaunchGeom g;
   if (!ring_geom(stage_bytes(o), o.nb, x_bf16 ? 2 : 3, g)) return cudaErrorNotSupported;
   a.ops = nullptr;
@@ -616,15 +653,7 @@ cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, 
   a.barrier = nullptr;
   a.err = device_error_ptr();
   a.pf = g_prefetch_stages;
-  switch (qtype * 4 + (x_bf16 ? 2 : 3)) {
-    case T_Q4_K * 4 + 2: return launch_prog<false, T_Q4_K, 2>(a, g, false, stream, pdl);
-    case T_Q4_K * 4 + 3: return launch_prog<false, T_Q4_K, 3>(a, g, false, stream, pdl);
-    case T_Q5_K * 4 + 2: return launch_prog<false, T_Q5_K, 2>(a, g, false, stream, pdl);
-    case T_Q5_K * 4 + 3: return launch_prog<false, T_Q5_K, 3>(a, g, false, stream, pdl);
-    case T_Q6_K * 4 + 2: return launch_prog<false, T_Q6_K, 2>(a, g, false, stream, pdl);
-    case T_Q6_K * 4 + 3: return launch_prog<false, T_Q6_K, 3>(a, g, false, stream, pdl);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_single(qtype, x_bf16 ? 2 : 3, o.R, a, g, stream, pdl);
 }
 
 // Plans the whole program on the host and returns the workspace bytes it
@@ -745,7 +774,7 @@ cudaError_t prog_run(const ProgPlan* plan, void* ws, cudaStream_t stream) {
   g.slot = plan->slot;
   g.smem = static_cast<size_t>(plan->smem);
   // grid barriers need every CTA resident: cooperative launch
-  return launch_prog<true, 0, 0>(a, g, plan->coop != 0, stream, plan->coop == 0);
+  return launch_prog<true, 0, 0, 4>(a, g, plan->coop != 0, stream, plan->coop == 0);
 }
 
 }  // namespace kq
