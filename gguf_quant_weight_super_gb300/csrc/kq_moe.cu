@@ -14,9 +14,12 @@
 //    and CTA (tile, d) takes the d-th one, e, with its pairs (token m, slot j)
 //    in (m, j) order.  The CTAs of tile 0 also write this plan to the
 //    workspace (expert of each rank, offsets, pairs) for inspection;
-//  * the CTA copies its 32 rows of expert e with one TMA bulk copy, then for
+//  * the CTA copies its tile of expert e (whole rows, as large as fits in
+//    100 KB: 256, 128 or 64 rows, a quad of lanes per 4, 2 or 1 of them; wider
+//    rows 32 or 16 rows, 2 or 4 quads per row) with one TMA bulk copy, then for
 //    each pair stages that pair's x as block-float limbs and applies the rows
 //    to it with the lane cores of kq_lane.cuh;
+//  * if no routed id is valid at all, the gated outputs are zero (empty sums);
 //  * without gate weights the result of pair (m, j) is row j of token m's
 //    output block (y[m][j][n]); with gate weights it goes to the workspace and
 //    the last CTA to finish the tile (arrival counter) writes
@@ -29,12 +32,14 @@ using namespace lane;
 
 namespace {
 
-constexpr int MT = 32;          // rows per tile
+constexpr int MT_MIN = 16;      // rows per tile at the most quads per row (sizes the tile counters)
+constexpr int kForcePhases = 0; // 0: quads per row chosen per shape
+constexpr int kForceRows = 0;   // 0: rows per quad chosen per shape
 constexpr int MW = 8;           // warps
 constexpr int MTH = MW * 32;
 constexpr int kMaxPairs = 512;  // M * top_k
 constexpr int kMaxExperts = 4096;
-constexpr int64_t kMaxTileBytes = 100 * 1024;
+constexpr int64_t kMaxTileBytes = 100 * 1024;  // 32 rows at most (API limit)
 
 struct MoeArgs {
   const uint8_t* W;
@@ -52,6 +57,7 @@ struct MoeArgs {
   int* cnt;   // per-tile arrival counters (gate case)
   float* part;
   int Dmax;
+  int nph, rq, rt;  // quads per row (block phases), rows per quad, rows per tile = 8 * MW * rq / nph
 };
 
 struct MoeSmem {
@@ -63,15 +69,17 @@ struct MoeSmem {
 
 __host__ __device__ inline size_t moe_ximg_offset() { return (sizeof(MoeSmem) + 16 + 127) & ~size_t(127); }
 
-// Row sum of one pair over the tile (lane quads: row 4w + (q >> 1), block phase q & 1).
-template <int QT, int NL>
-__device__ __forceinline__ float pair_rows(uint32_t tile_s, int64_t row_bytes, int nb, const XImg& xi, int rit,
-                                           int ph, int c, const ScaleLane& sl) {
+// Row sums of one pair over the tile for the RQ rows of this quad (rows
+// rp, rp + rstride, ...; nph quads per row, the quad of phase ph taking blocks
+// ph, ph + nph, ...): each block's x slice is loaded once for all RQ rows.
+template <int QT, int NL, int RQ>
+__device__ __forceinline__ void pair_rows(uint32_t rp, uint32_t rstride, int nb, const XImg& xi, int ph, int nph,
+                                          int c, const ScaleLane& sl, float (&acc)[4]) {
   constexpr int BB = Fmt<QT>::BYTES;
   const int xoff = (QT == T_Q6_K) ? (40 * (c >> 1) + 4 * (c & 1)) : 20 * c;
-  const uint32_t rp = tile_s + static_cast<uint32_t>(rit * row_bytes);
-  float acc = 0.0f;
-  for (int b = ph; b < nb; b += 2) {
+#pragma unroll
+  for (int i = 0; i < RQ; ++i) acc[i] = 0.0f;
+  for (int b = ph; b < nb; b += nph) {
     XSlice<NL> X;
     load_slice<QT, NL>(xi.limb_s + 4 * (b * XWB + xoff), 4 * xi.plane, X);
     const float s = __uint_as_float(lds32(xi.scale_s + 4 * (2 * b + (c >> 1))));
@@ -79,17 +87,23 @@ __device__ __forceinline__ float pair_rows(uint32_t tile_s, int64_t row_bytes, i
       const uint4 sv = lds128(xi.si16q_s + 4 * (16 * b + 4 * c));
       const int4 si = make_int4(static_cast<int>(sv.x), static_cast<int>(sv.y), static_cast<int>(sv.z),
                                 static_cast<int>(sv.w));
-      acc = core_q6<NL>(rp + b * BB, X, si, s, c, acc);
+#pragma unroll
+      for (int i = 0; i < RQ; ++i) acc[i] = core_q6<NL>(rp + i * rstride + b * BB, X, si, s, c, acc[i]);
     } else {
       const uint2 sv = lds64(xi.si32_s + 4 * (8 * b + 2 * c));
-      acc = core_q45<QT, NL>(rp + b * BB, X, make_int2(static_cast<int>(sv.x), static_cast<int>(sv.y)), s, c, sl,
-                             acc);
+      const int2 si = make_int2(static_cast<int>(sv.x), static_cast<int>(sv.y));
+#pragma unroll
+      for (int i = 0; i < RQ; ++i) acc[i] = core_q45<QT, NL>(rp + i * rstride + b * BB, X, si, s, c, sl, acc[i]);
     }
   }
-  acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, 1));
-  acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, 2));
-  acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, 4));
-  return acc;
+#pragma unroll
+  for (int i = 0; i < RQ; ++i) {
+    float v = acc[i];
+    v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+    v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+    for (int o = 4; o < 4 * nph; o <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    acc[i] = v;
+  }
 }
 
 template <int QT, int NL>
@@ -147,11 +161,17 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
   }
   __syncthreads();
   const int e = sm.misc[0], D = sm.misc[1];
+  if (D == 0 && a.gate && d == 0) {  // no valid pair at all: the gated outputs of this tile are zero
+    const int64_t r0 = static_cast<int64_t>(tile) * a.rt;
+    const int nrows = static_cast<int>(min_i64(a.rt, a.N - r0));
+    for (int i = tid; i < a.M * nrows; i += MTH)
+      a.y[static_cast<int64_t>(i / nrows) * a.N + r0 + i % nrows] = 0.0f;
+  }
   if (e < 0) return;  // fewer distinct experts than this rank
 
   // ---- the expert's tile: one bulk copy of whole rows
-  const int64_t r0 = static_cast<int64_t>(tile) * MT;
-  const int nrows = static_cast<int>(min_i64(MT, a.N - r0));
+  const int64_t r0 = static_cast<int64_t>(tile) * a.rt;
+  const int nrows = static_cast<int>(min_i64(a.rt, a.N - r0));
   const uint8_t* src = a.W + e * a.expert_bytes + r0 * a.row_bytes;
   const uintptr_t s0 = reinterpret_cast<uintptr_t>(src);
   const uintptr_t as = s0 & ~uintptr_t(15), ae = (s0 + nrows * a.row_bytes + 15) & ~uintptr_t(15);
@@ -187,11 +207,13 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
     }
   }
 
-  // ---- apply the rows to every pair
+  // ---- apply the rows to every pair: quad rows rq0 + i * (64 / nph), i < rq
   const int quad = lane >> 2, c = lane & 3;
-  const int rit = 4 * warp + (quad >> 1), ph = quad & 1;
+  const int rq0 = warp * (8 / a.nph) + quad / a.nph, ph = quad % a.nph;
+  const int rstep = 8 * MW / a.nph;
   const ScaleLane sl = scale_lane(c);
-  const uint32_t tile_s = smem_u32(tile_buf) + static_cast<uint32_t>(s0 - as);
+  const uint32_t rp = smem_u32(tile_buf) + static_cast<uint32_t>(s0 - as) + static_cast<uint32_t>(rq0 * a.row_bytes);
+  const uint32_t rstride = static_cast<uint32_t>(rstep * a.row_bytes);
   bool ok = true;
   for (int j = 0; j < np; ++j) {
     const int pr = sm.pairs[j];
@@ -203,10 +225,15 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
     stage_x<NL, MTH>(xp, NL == 2, a.K, a.nb, xi, tid);
     __syncthreads();
     if (j == 0) ok = mbar_wait(bar, 0, a.err);
-    const float v = pair_rows<QT, NL>(tile_s, a.row_bytes, a.nb, xi, rit, ph, c, sl);
-    if (ok && c == 0 && ph == 0 && rit < nrows) {
-      if (a.gate) a.part[static_cast<int64_t>(pr) * a.N + r0 + rit] = v;
-      else a.y[static_cast<int64_t>(pr) * a.N + r0 + rit] = v;
+    float v[4];
+    if (a.rq == 4) pair_rows<QT, NL, 4>(rp, rstride, a.nb, xi, ph, a.nph, c, sl, v);
+    else if (a.rq == 2) pair_rows<QT, NL, 2>(rp, rstride, a.nb, xi, ph, a.nph, c, sl, v);
+    else pair_rows<QT, NL, 1>(rp, rstride, a.nb, xi, ph, a.nph, c, sl, v);
+    if (ok && c == 0 && ph == 0) {
+      float* out = (a.gate ? a.part : a.y) + static_cast<int64_t>(pr) * a.N + r0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (i < a.rq && rq0 + i * rstep < nrows) out[rq0 + i * rstep] = v[i];
     }
   }
   if (np == 0 && tid == 0) ok = mbar_wait(bar, 0, a.err);  // the copy must land before the CTA exits
@@ -221,12 +248,21 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
   __threadfence();
   for (int i = tid; i < a.M * nrows; i += MTH) {
     const int m = i / nrows, r = i - m * nrows;
+    const float* pp = a.part + static_cast<int64_t>(m) * a.top_k * a.N + r0 + r;
+    const int* id = sm.ids + m * a.top_k;
+    const float* g = a.gate + m * a.top_k;
     float v = 0.0f;
-    for (int s = 0; s < a.top_k; ++s) {
-      const int pr = m * a.top_k + s;
-      if (sm.ids[pr] < 0) continue;  // dropped pair (bad id)
-      v = __fmaf_rn(a.gate[pr], __ldcg(a.part + static_cast<int64_t>(pr) * a.N + r0 + r), v);
+    int j = 0;
+    for (; j + 4 <= a.top_k; j += 4) {  // four loads in flight, applied in slot order; dropped pairs skipped
+      float p[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) p[q] = id[j + q] >= 0 ? __ldcg(pp + static_cast<int64_t>(j + q) * a.N) : 0.0f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (id[j + q] >= 0) v = __fmaf_rn(g[j + q], p[q], v);
     }
+    for (; j < a.top_k; ++j)
+      if (id[j] >= 0) v = __fmaf_rn(g[j], __ldcg(pp + static_cast<int64_t>(j) * a.N), v);
     a.y[static_cast<int64_t>(m) * a.N + r0 + r] = v;
   }
   if (tid == 0) a.cnt[tile] = 0;  // ready for the next call
@@ -257,13 +293,28 @@ cudaError_t launch_moe_t(const MoeArgs& a, size_t smem, cudaStream_t st) {
 
 size_t a256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Tile shape: the largest tile of at most kMaxTileBytes, from 256 rows (a quad per
+// 4 rows, each block's x slice serving all 4) down to 16 rows (4 quads per row).
+// Fewer, larger tiles mean fewer CTAs paying the fixed costs (grouping, copy
+// latency, x staging) per byte of weights.
+void moe_tile_shape(int64_t row_bytes, int& nph, int& rq) {
+  nph = 4;
+  rq = 1;
+  for (int r = 4; r >= 1; r >>= 1)
+    if (8 * MW * r * row_bytes + 32 <= kMaxTileBytes) { nph = 1; rq = r; break; }
+  if (nph == 4 && 8 * MW / 2 * row_bytes + 32 <= kMaxTileBytes) nph = 2;
+  if (kForcePhases) nph = kForcePhases;
+  if (kForceRows) rq = kForceRows;
+  if (nph > 1) rq = 1;
+}
+
 }  // namespace
 
 MoeLayout moe_layout(int64_t N, int64_t M, int top_k, int n_experts) {
   MoeLayout L;
   const int64_t MK = M * top_k;
   L.Dmax = static_cast<int>(MK < n_experts ? MK : n_experts);
-  L.ntiles = (N + MT - 1) / MT;
+  L.ntiles = (N + MT_MIN - 1) / MT_MIN;  // the most tiles any rows-per-tile choice makes
   L.plan_off = 256;
   L.cnt_off = L.plan_off + a256(sizeof(int) * (1 + 2 * static_cast<size_t>(L.Dmax) + 1 + MK));
   L.part_off = L.cnt_off + a256(sizeof(int) * static_cast<size_t>(L.ntiles));
@@ -275,7 +326,7 @@ bool moe_supported(int qtype, int64_t K, int64_t M, int top_k, int n_experts) {
   const int BB = block_bytes_of(qtype);
   const int64_t row_bytes = ((K + 255) / 256) * BB;
   return BB && M * top_k <= kMaxPairs && n_experts <= kMaxExperts && (K + 255) / 256 <= 64 &&
-         MT * row_bytes + 32 <= kMaxTileBytes;
+         32 * row_bytes + 32 <= kMaxTileBytes;
 }
 
 cudaError_t launch_moe_err(int qtype, const void* W, int n_experts, const int32_t* ids, const float* gate,
@@ -296,7 +347,6 @@ cudaError_t launch_moe_err(int qtype, const void* W, int n_experts, const int32_
   a.n_experts = n_experts;
   a.M = M;
   a.top_k = top_k;
-  a.ntiles = static_cast<int>(L.ntiles);
   a.ids = ids;
   a.gate = gate;
   a.x = x;
@@ -307,8 +357,11 @@ cudaError_t launch_moe_err(int qtype, const void* W, int n_experts, const int32_
   a.part = reinterpret_cast<float*>(w + L.part_off);
   a.Dmax = L.Dmax;
   const int NL = x_bf16 ? 2 : 3;
+  moe_tile_shape(a.row_bytes, a.nph, a.rq);
+  a.rt = 8 * MW * a.rq / a.nph;
+  a.ntiles = static_cast<int>((N + a.rt - 1) / a.rt);
   const size_t smem = moe_ximg_offset() + ((ximg_bytes(a.nb, NL) + 127) & ~size_t(127)) +
-                      static_cast<size_t>(MT * a.row_bytes + 32);
+                      static_cast<size_t>(a.rt * a.row_bytes + 32);
   if (smem > static_cast<size_t>(kMaxSmemPerBlock)) return cudaErrorNotSupported;
   switch (qtype * 4 + NL) {
     case T_Q4_K * 4 + 2: return launch_moe_t<T_Q4_K, 2>(a, smem, st);

@@ -128,6 +128,20 @@ def test_moe_bad_ids_are_dropped_and_reported():
             assert _rel(yg, yr, sr, mask=~bad) <= TOL["bf16"]
 
 
+def test_moe_all_ids_bad_gives_zero_gated_output():
+    """Every routed id out of range: no pair survives, every gated output is the
+    empty sum (0), and the bad ids are reported."""
+    E, N, K, M, top_k = 8, 80, 512, 3, 2
+    ids = np.array([[8, -1], [9, 100], [-5, 8]], dtype=np.int32)
+    We, ids_, gate, x, ws, y, args = _moe(Q4_K, E, N, K, M, top_k, "f32", True, 406, ids=ids)
+    y.fill_(np.nan)
+    kq.kq_moe_matvec(*args)
+    with pytest.raises(kq.KQError) as ex:
+        kq.kq_moe_check(ws)
+    assert ex.value.status == -8
+    assert torch.count_nonzero(y).item() == 0
+
+
 def test_moe_reads_only_routed_experts_and_repeats_identically():
     """Unrouted experts hold blocks whose d is NaN: any use of them would
     poison the outputs.  Repeated calls give identical outputs (the arrival
