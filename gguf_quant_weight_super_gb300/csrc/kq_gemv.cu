@@ -64,6 +64,9 @@ constexpr int CONSUMER_BAR = 1;        // named barrier of the consumer warps
 constexpr int MAX_NB = 64;             // K <= 16384
 // Largest stage (32 row segments): 48 KB keeps a ring of at least 4 slots.
 constexpr int64_t kSlotCap = 48 * 1024;
+// Largest stage of whole rows (one bulk copy), by rows per quad: a taller
+// tile (more x reuse) may take a larger stage and a shorter ring.
+__host__ __device__ constexpr int64_t whole_cap(int R) { return R >= 4 ? 72 * 1024 : R == 2 ? 56 * 1024 : 48 * 1024; }
 
 }  // namespace
 
@@ -74,7 +77,7 @@ struct KqOp {
   float* y;
   float* part;       // split K: partial row sums [KS][ntiles*TT] (workspace), else null
   int32_t R;         // rows per quad: a tile is 8R rows (programs: R = 4)
-  int32_t pad0;
+  int32_t contig;    // stages are whole rows, copied as one block (row stride in a stage = row_bytes)
   int64_t N;
   int64_t row_bytes;
   int32_t K, nb, type, x_bf16;
@@ -94,7 +97,8 @@ struct ProgArgs {
   int nb_max, nl_max;
   int* barrier;      // grid barrier arrivals (programs with OP_WAIT), zero at launch
   int* err;
-  int pf;            // L2 prefetch distance in stages
+  int pf;            // L2 prefetch distance in stages (0: none)
+  int inflight;      // stages in flight at most (0: as many as the ring holds)
   int final_fix;     // split-K sums remain after the last op: final grid barrier
 };
 
@@ -113,10 +117,22 @@ __device__ __forceinline__ int first_unit(const KqOp& o, int cta, int G) {
 }
 
 // Producer: lane i copies row i's segment (blocks [b0, b0+n)) of the tile
-// into slot + i*srb, as its 16-byte aligned superset; arrive on full.
+// into slot + i*srb, as its 16-byte aligned superset; arrive on full.  A
+// stage of whole rows is one contiguous block: lane 0 copies its 16-byte
+// aligned superset with one bulk copy (fewer, larger copies stream faster).
 __device__ __forceinline__ void produce(const KqOp& o, int tile, int b0, int n, uint8_t* slot, uint64_t* full,
                                        int lane, int BB) {
   const int64_t r0 = static_cast<int64_t>(tile) * (8 * o.R);
+  if (o.contig) {
+    if (lane == 0) {
+      const int64_t nrows = min_i64(8 * o.R, o.N - r0);
+      const uintptr_t s0 = reinterpret_cast<uintptr_t>(o.W + r0 * o.row_bytes);
+      const uintptr_t as = s0 & ~uintptr_t(15), ae = (s0 + nrows * o.row_bytes + 15) & ~uintptr_t(15);
+      mbar_arrive_expect_tx(full, static_cast<uint32_t>(ae - as));
+      bulk_g2s(slot, reinterpret_cast<const void*>(as), static_cast<uint32_t>(ae - as), full);
+    }
+    return;
+  }
   uint32_t len = 0;
   const uint8_t* src = nullptr;
   if (lane < 8 * o.R && r0 + lane < o.N) {
@@ -206,7 +222,9 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
         for (int i = 0; i < R; ++i) {
           const int r = quad + 8 * i;
           // W is 16-byte aligned: the segment's offset in its 16-byte granule
-          const uint32_t off = (seg0 + static_cast<uint32_t>(r) * static_cast<uint32_t>(o.row_bytes)) & 15u;
+          // (one offset for a stage copied as one block)
+          const uint32_t off =
+              (seg0 + (o.contig ? 0u : static_cast<uint32_t>(r) * static_cast<uint32_t>(o.row_bytes))) & 15u;
           rp[i] = sp + r * o.srb + off + bi * BB;
         }
         for (; bi < n; bi += NC) {
@@ -331,9 +349,20 @@ __device__ __forceinline__ void cur_next(const ProgArgs& a, StageCursor& c, int 
   ++c.oi;
   cur_seek<PROG>(a, c, cta, G);
 }
-// L2 prefetch of a stage's row segments (lane i: row i).
+// L2 prefetch of a stage's row segments (lane i: row i; a contiguous stage:
+// lane 0, one prefetch).
 __device__ __forceinline__ void prefetch_stage(const StageCursor& c, int lane) {
   const int BB = block_bytes_of(c.o.type);
+  if (c.o.contig) {
+    const int64_t r0 = static_cast<int64_t>(c.tile) * (8 * c.o.R);
+    if (lane == 0) {
+      const int64_t nrows = min_i64(8 * c.o.R, c.o.N - r0);
+      const uintptr_t s0 = reinterpret_cast<uintptr_t>(c.o.W + r0 * c.o.row_bytes);
+      const uintptr_t as = s0 & ~uintptr_t(15), ae = (s0 + nrows * c.o.row_bytes + 15) & ~uintptr_t(15);
+      bulk_prefetch_l2(reinterpret_cast<const void*>(as), static_cast<uint32_t>(ae - as));
+    }
+    return;
+  }
   const int n = min(c.o.KC, c.kb1 - c.b0);
   const int64_t row = static_cast<int64_t>(c.tile) * (8 * c.o.R) + lane;
   if (lane < 8 * c.o.R && row < c.o.N) {
@@ -390,7 +419,12 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
         const bool ok = mbar_wait(&rg.empty[slot], static_cast<uint32_t>((q / a.S - 1) & 1), a.err);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
       }
-      if (pc.valid) {  // ask L2 for the stage a.pf stages ahead
+      if (a.inflight && q >= a.inflight) {  // keep the memory queues short: stage q - inflight has landed
+        const int64_t r = q - a.inflight;
+        const bool ok = mbar_wait(&rg.full[r % a.S], static_cast<uint32_t>((r / a.S) & 1), a.err);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      }
+      if (a.pf > 0 && pc.valid) {  // ask L2 for the stage a.pf stages ahead
         prefetch_stage(pc, lane);
         cur_next<PROG>(a, pc, cta, G);
       }
@@ -508,10 +542,15 @@ bool plan_op(KqOp& o, int G, bool allow_split, int64_t slot_cap, bool allow_shor
   o.row_bytes = static_cast<int64_t>(o.nb) * BB;
   // tile height 8R: the busiest CTA's rows, rounds * 8R, with shorter tiles
   // charged for their lost x reuse (one x slice serves R rows)
+  // Heights whose tile of whole rows fits one slot are preferred: such a
+  // stage is one bulk copy (per-row copies of short segments stream slower).
   o.R = 4;
   if (allow_short_tiles) {
+    bool any_whole = false;
+    for (int r : {4, 2, 1}) any_whole = any_whole || 8 * r * o.row_bytes + 32 <= whole_cap(r);
     double best = -1.0;
     for (int r : {4, 2, 1}) {
+      if (any_whole && 8 * r * o.row_bytes + 32 > whole_cap(r)) continue;
       const int64_t nt = (o.N + 8 * r - 1) / (8 * r);
       const double cost = static_cast<double>((nt + G - 1) / G) * 8 * r * (1.0 + 0.08 * (4 / r - 1));
       if (best < 0 || cost < best - 1e-9) { best = cost; o.R = r; }
@@ -521,8 +560,9 @@ bool plan_op(KqOp& o, int G, bool allow_split, int64_t slot_cap, bool allow_shor
   const int64_t ntiles = (o.N + TTo - 1) / TTo;
   if (ntiles > (int64_t(1) << 28)) return false;
   int kcmax = o.nb;
-  while (kcmax > 1 && static_cast<int64_t>(TTo) * seg_stride(o.type, kcmax) > slot_cap) --kcmax;
-  if (static_cast<int64_t>(TTo) * seg_stride(o.type, kcmax) > slot_cap) return false;
+  const bool whole = static_cast<int64_t>(TTo) * o.row_bytes + 32 <= whole_cap(o.R);
+  while (!whole && kcmax > 1 && static_cast<int64_t>(TTo) * seg_stride(o.type, kcmax) > slot_cap) --kcmax;
+  if (!whole && static_cast<int64_t>(TTo) * seg_stride(o.type, kcmax) > slot_cap) return false;
   // K-parts (with a workspace): minimise the busiest CTA's blocks,
   // ceil(tiles*KS / G) * ceil(nb / KS), plus one block per split level
   int KS = 1;
@@ -539,12 +579,17 @@ bool plan_op(KqOp& o, int G, bool allow_split, int64_t slot_cap, bool allow_shor
   const int nst = (o.kpb + kcmax - 1) / kcmax;
   o.KC = (o.kpb + nst - 1) / nst;
   o.srb = seg_stride(o.type, o.KC);
+  // whole rows per stage: one copy per stage, rows at their memory stride
+  o.contig = (o.KS == 1 && o.KC == o.nb) ? 1 : 0;
+  if (o.contig) o.srb = static_cast<int32_t>(o.row_bytes);
   o.ntiles = static_cast<int32_t>(ntiles);
   o.nunits = static_cast<int32_t>(ntiles * KS);
   return true;
 }
 
-int64_t stage_bytes(const KqOp& o) { return static_cast<int64_t>(8 * o.R) * o.srb; }
+// A contiguous stage adds 16 bytes of alignment and 16 of read slack (Q6_K's
+// unaligned reads); a per-row stage has both inside its row stride.
+int64_t stage_bytes(const KqOp& o) { return static_cast<int64_t>(8 * o.R) * o.srb + (o.contig ? 32 : 0); }
 
 struct LaunchGeom {
   int S, slot;
@@ -604,7 +649,8 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 }  // namespace
 
 namespace {
-int g_prefetch_stages = 8;  // L2 prefetch distance (stages beyond the one being copied)
+int g_prefetch_stages = 0;  // L2 prefetch distance (stages beyond the one being copied; 0: none)
+int g_max_inflight = 0;     // stages in flight per CTA at most (0: the ring's slots)
 
 template <int QT, int NL>
 cudaError_t launch_single_r(int R, ProgArgs& a, const LaunchGeom& g, cudaStream_t st, bool pdl) {
@@ -653,6 +699,7 @@ cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, 
   a.barrier = nullptr;
   a.err = device_error_ptr();
   a.pf = g_prefetch_stages;
+  a.inflight = g_max_inflight;
   return launch_single(qtype, x_bf16 ? 2 : 3, o.R, a, g, stream, pdl);
 }
 
@@ -769,6 +816,7 @@ cudaError_t prog_run(const ProgPlan* plan, void* ws, cudaStream_t stream) {
   a.final_fix = plan->final_fix;
   a.err = device_error_ptr();
   a.pf = g_prefetch_stages;
+  a.inflight = g_max_inflight;
   LaunchGeom g;
   g.S = plan->S;
   g.slot = plan->slot;
