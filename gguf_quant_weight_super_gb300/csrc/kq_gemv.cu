@@ -149,13 +149,19 @@ __device__ __forceinline__ void produce(const KqOp& o, int tile, int b0, int n, 
   if (len) bulk_g2s(slot + lane * o.srb, src, len, full);
 }
 
-// Bounded wait until the grid-wide arrival counter reaches target.
+// Grid barrier arrival: a release add (cumulative: it publishes every write
+// the CTA's consumers made before the consumer barrier that precedes it).
+__device__ __forceinline__ void grid_arrive(int* counter) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(counter) : "memory");
+}
+
+// Bounded wait until the grid-wide arrival counter reaches target (acquire
+// loads; the consumer barrier that follows extends the order to the CTA).
 __device__ __forceinline__ bool grid_wait(const int* counter, int target, int* err) {
-  for (uint32_t i = 0; i < (1u << 26); ++i) {
+  for (uint32_t i = 0; i < (1u << 23); ++i) {
     int v;
     asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
     if (v >= target) return true;
-    __nanosleep(64);
   }
   record_error(err, DEV_ERR_MBAR_TIMEOUT);
   return false;
@@ -455,12 +461,10 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
       consumer_sync();
       ++barriers;
       if (ctid == 0) {
-        __threadfence();
-        atomicAdd(a.barrier, 1);
+        grid_arrive(a.barrier);
         grid_wait(a.barrier, barriers * G, a.err);  // on timeout the error word is set
       }
       consumer_sync();
-      __threadfence();
       // split-K sums of the ops finished so far (no later op reads them: the
       // host plans no split for an op whose output feeds a later x)
       if constexpr (PROG) {
@@ -494,12 +498,10 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
     if (a.final_fix) {
       ++barriers;
       if (ctid == 0) {
-        __threadfence();
-        atomicAdd(a.barrier, 1);
+        grid_arrive(a.barrier);
         grid_wait(a.barrier, barriers * G, a.err);
       }
       consumer_sync();
-      __threadfence();
       if constexpr (PROG) {
         for (; fixed < a.n_ops; ++fixed) {
           const KqOp f = load_op<PROG>(a, fixed);
