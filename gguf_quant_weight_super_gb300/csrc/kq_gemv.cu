@@ -98,7 +98,6 @@ struct ProgArgs {
   int* barrier;      // grid barrier arrivals (programs with OP_WAIT), zero at launch
   int* err;
   int pf;            // L2 prefetch distance in stages (0: none)
-  int inflight;      // stages in flight at most (0: as many as the ring holds)
   int final_fix;     // split-K sums remain after the last op: final grid barrier
 };
 
@@ -183,9 +182,10 @@ struct Red {
 };
 // Running position of the consumers (identical in every consumer warp).
 struct Walk {
-  int64_t q;     // stages consumed
-  int64_t us;    // units finished
-  int cb;        // blocks seen, mod NC: chunk-to-warp rotation
+  int slot;        // ring slot of the next stage
+  uint32_t phase;  // parity of the ring lap of the next stage
+  int rs;          // reduction buffer of the next unit
+  int cb;          // blocks seen, mod NC: chunk-to-warp rotation
   bool failed;
 };
 
@@ -211,9 +211,9 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
     for (int i = 0; i < R; ++i) acc[i] = 0.0f;
     for (int b0 = kb0; b0 < kb1; b0 += o.KC) {
       const int n = min(o.KC, kb1 - b0);
-      const int slot = static_cast<int>(wk.q % rg.S);
+      const int slot = wk.slot;
       if (!wk.failed) {
-        const bool ok = mbar_wait(&rg.full[slot], static_cast<uint32_t>((wk.q / rg.S) & 1), err);
+        const bool ok = mbar_wait(&rg.full[slot], wk.phase, err);
         wk.failed = !__all_sync(0xFFFFFFFFu, ok);
       }
       int bi = warp - wk.cb;
@@ -257,7 +257,7 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
       wk.cb = (wk.cb + n) % NC;
       __syncwarp();
       if (lane == 0) mbar_arrive(&rg.empty[slot]);
-      ++wk.q;
+      if (++wk.slot == rg.S) { wk.slot = 0; wk.phase ^= 1u; }
     }
     // this warp's partial row sums: over the quad's lanes, then to shared memory
 #pragma unroll
@@ -265,8 +265,8 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
       acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xFFFFFFFFu, acc[i], 1));
       acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xFFFFFFFFu, acc[i], 2));
     }
-    const int rs = static_cast<int>(wk.us % rd.RS);
-    ++wk.us;
+    const int rs = wk.rs;
+    if (++wk.rs == rd.RS) wk.rs = 0;
     float* rb = rd.buf + static_cast<size_t>(rs) * NC * TT;
     if (c == 0) {
 #pragma unroll
@@ -414,20 +414,15 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
   if (warp == NC) {
     // ------------------------------------------------------------ producer
     pdl_launch_dependents();
-    int64_t q = 0;
+    int q = 0, slot = 0;
+    uint32_t lap = 0;  // parity of the ring lap
     StageCursor cc, pc;
     cur_start<PROG>(a, cc, cta, G);
     pc = cc;
     for (int k = 0; k < a.pf && pc.valid; ++k) cur_next<PROG>(a, pc, cta, G);
     while (cc.valid) {
-      const int slot = static_cast<int>(q % a.S);
-      if (q >= a.S) {
-        const bool ok = mbar_wait(&rg.empty[slot], static_cast<uint32_t>((q / a.S - 1) & 1), a.err);
-        if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      }
-      if (a.inflight && q >= a.inflight) {  // keep the memory queues short: stage q - inflight has landed
-        const int64_t r = q - a.inflight;
-        const bool ok = mbar_wait(&rg.full[r % a.S], static_cast<uint32_t>((r / a.S) & 1), a.err);
+      if (q >= a.S) {  // the slot's previous stage has been consumed
+        const bool ok = mbar_wait(&rg.empty[slot], lap ^ 1u, a.err);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
       }
       if (a.pf > 0 && pc.valid) {  // ask L2 for the stage a.pf stages ahead
@@ -438,10 +433,11 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
               &rg.full[slot], lane, block_bytes_of(cc.o.type));
       cur_next<PROG>(a, cc, cta, G);
       ++q;
+      if (++slot == a.S) { slot = 0; lap ^= 1u; }
     }
     // leave only after the copies in flight have landed (bounded)
     if (lane == 0)
-      for (int64_t r = (q > a.S ? q - a.S : 0); r < q; ++r)
+      for (int r = (q > a.S ? q - a.S : 0); r < q; ++r)
         mbar_wait(&rg.full[r % a.S], static_cast<uint32_t>((r / a.S) & 1), nullptr);
     return;
   }
@@ -450,13 +446,27 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
   pdl_wait();
   pdl_launch_dependents();
   const int ctid = threadIdx.x;
-  Walk wk = {0, 0, 0, false};
+  Walk wk = {0, 0u, 0, 0, false};
   int barriers = 0;
-  int fixed = 0;  // ops before this index have their split-K sums added
+  // Split-K sums: no later op reads them (the host plans no split for an op
+  // whose output feeds a later x), so the sums of the ops before the last
+  // barrier passed are added just before the next barrier, off the path from
+  // a barrier to the next op's first product (CTAs that finish early do it
+  // while the rest of the grid finishes).
+  int fixed = 0;     // ops before this index have their split-K sums added
+  int complete = 0;  // ops before this index have all their partial sums written
+  KqOp nxt = load_op<PROG>(a, 0);  // the next op's descriptor, loaded one op ahead
   for (int oi = 0; oi < a.n_ops; ++oi) {
-    const KqOp o = load_op<PROG>(a, oi);
+    const KqOp o = nxt;
+    if (PROG && oi + 1 < a.n_ops) nxt = load_op<PROG>(a, oi + 1);
     const int NL = o.x_bf16 ? 2 : 3;
     if (oi > 0 && (o.flags & OP_WAIT)) {
+      if constexpr (PROG) {
+        for (; fixed < complete; ++fixed) {
+          const KqOp f = load_op<PROG>(a, fixed);
+          if (f.KS > 1) fixup_op(f, cta, G, ctid);
+        }
+      }
       // publish this CTA's outputs so far, then wait for the rest of the grid
       consumer_sync();
       ++barriers;
@@ -465,14 +475,7 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
         grid_wait(a.barrier, barriers * G, a.err);  // on timeout the error word is set
       }
       consumer_sync();
-      // split-K sums of the ops finished so far (no later op reads them: the
-      // host plans no split for an op whose output feeds a later x)
-      if constexpr (PROG) {
-        for (; fixed < oi; ++fixed) {
-          const KqOp f = load_op<PROG>(a, fixed);
-          if (f.KS > 1) fixup_op(f, cta, G, ctid);
-        }
-      }
+      complete = oi;
     }
     const XImg xi = ximg_at(xbase, a.nb_max, a.nl_max);
     if constexpr (!PROG) {
@@ -491,9 +494,16 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
     if (NL == 2) consume_any<2>(o, xi, rg, rd, wk, a.err, cta, G);
     else consume_any<3>(o, xi, rg, rd, wk, a.err, cta, G);
   }
+  if constexpr (PROG) {  // sums complete since the last barrier
+    for (; fixed < complete; ++fixed) {
+      const KqOp f = load_op<PROG>(a, fixed);
+      if (f.KS > 1) fixup_op(f, cta, G, ctid);
+    }
+  }
   if (a.barrier) {
-    // final barrier (only when split-K sums remain), then the exit count: the
-    // last CTA to leave resets both counters for the next launch
+    // final barrier (only when split-K sums of the last stage remain), then
+    // the exit count: the last CTA to leave resets both counters for the next
+    // launch
     consumer_sync();
     if (a.final_fix) {
       ++barriers;
@@ -652,7 +662,6 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 namespace {
 int g_prefetch_stages = 0;  // L2 prefetch distance (stages beyond the one being copied; 0: none)
-int g_max_inflight = 0;     // stages in flight per CTA at most (0: the ring's slots)
 
 template <int QT, int NL>
 cudaError_t launch_single_r(int R, ProgArgs& a, const LaunchGeom& g, cudaStream_t st, bool pdl) {
@@ -701,7 +710,6 @@ cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, 
   a.barrier = nullptr;
   a.err = device_error_ptr();
   a.pf = g_prefetch_stages;
-  a.inflight = g_max_inflight;
   return launch_single(qtype, x_bf16 ? 2 : 3, o.R, a, g, stream, pdl);
 }
 
@@ -818,7 +826,6 @@ cudaError_t prog_run(const ProgPlan* plan, void* ws, cudaStream_t stream) {
   a.final_fix = plan->final_fix;
   a.err = device_error_ptr();
   a.pf = g_prefetch_stages;
-  a.inflight = g_max_inflight;
   LaunchGeom g;
   g.S = plan->S;
   g.slot = plan->slot;
