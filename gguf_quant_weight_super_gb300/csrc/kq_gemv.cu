@@ -44,6 +44,9 @@
 //    resident: cooperative launch) before its x is read; single products
 //    instead use programmatic dependent launch, streaming weights before
 //    griddepcontrol.wait.
+#include <algorithm>
+#include <vector>
+
 #include "kq_lane.cuh"
 
 namespace kq {
@@ -543,6 +546,35 @@ int seg_stride(int type, int kc) {
   return srb;
 }
 
+// Widest stage (blocks) of an op of tile height 8R: whole rows if they fit a
+// whole-row stage, else the widest row segments that fit a slot (0: none).
+int op_kcmax(const KqOp& o, int64_t slot_cap) {
+  const int TTo = 8 * o.R;
+  if (static_cast<int64_t>(TTo) * o.row_bytes + 32 <= whole_cap(o.R)) return o.nb;
+  int kcmax = o.nb;
+  while (kcmax > 1 && static_cast<int64_t>(TTo) * seg_stride(o.type, kcmax) > slot_cap) --kcmax;
+  return static_cast<int64_t>(TTo) * seg_stride(o.type, kcmax) > slot_cap ? 0 : kcmax;
+}
+
+// Whether nb blocks split into KS parts of ceil(nb/KS) >= 2 blocks, none empty.
+bool split_ok(int nb, int KS) {
+  const int kpb = (nb + KS - 1) / KS;
+  return KS == 1 || (kpb >= 2 && (KS - 1) * kpb < nb);
+}
+
+// K-parts KS of an op (planned tiles) and its stages: as few as fit, evened out.
+void set_split(KqOp& o, int KS, int kcmax) {
+  o.KS = KS;
+  o.kpb = (o.nb + KS - 1) / KS;
+  const int nst = (o.kpb + kcmax - 1) / kcmax;
+  o.KC = (o.kpb + nst - 1) / nst;
+  o.srb = seg_stride(o.type, o.KC);
+  // whole rows per stage: one copy per stage, rows at their memory stride
+  o.contig = (o.KS == 1 && o.KC == o.nb) ? 1 : 0;
+  if (o.contig) o.srb = static_cast<int32_t>(o.row_bytes);
+  o.nunits = static_cast<int32_t>(static_cast<int64_t>(o.ntiles) * KS);
+}
+
 // Geometry of one op: K-parts KS (only with a workspace) and stage width KC.
 // cost = block-chunks of the busiest CTA (a chunk = one block for 32 rows,
 // dealt to one warp), plus a fixed cost per stage and per split.
@@ -571,36 +603,23 @@ bool plan_op(KqOp& o, int G, bool allow_split, int64_t slot_cap, bool allow_shor
   const int TTo = 8 * o.R;
   const int64_t ntiles = (o.N + TTo - 1) / TTo;
   if (ntiles > (int64_t(1) << 28)) return false;
-  int kcmax = o.nb;
-  const bool whole = static_cast<int64_t>(TTo) * o.row_bytes + 32 <= whole_cap(o.R);
-  while (!whole && kcmax > 1 && static_cast<int64_t>(TTo) * seg_stride(o.type, kcmax) > slot_cap) --kcmax;
-  if (!whole && static_cast<int64_t>(TTo) * seg_stride(o.type, kcmax) > slot_cap) return false;
+  o.ntiles = static_cast<int32_t>(ntiles);
+  const int kcmax = op_kcmax(o, slot_cap);
+  if (kcmax < 1) return false;
   // K-parts (with a workspace): minimise the busiest CTA's blocks,
   // ceil(tiles*KS / G) * ceil(nb / KS), plus one block per split level
   int KS = 1;
   int64_t best = ((ntiles + G - 1) / G) * o.nb;
   for (int k2 = 2; allow_split && k2 <= 8; k2 *= 2) {
+    if (!split_ok(o.nb, k2)) break;
     const int kpb2 = (o.nb + k2 - 1) / k2;
-    if (kpb2 < 2 || (k2 - 1) * kpb2 >= o.nb) break;
     const int64_t c = ((ntiles * k2 + G - 1) / G) * kpb2 + (k2 / 2);
     if (c < best) { best = c; KS = k2; }
   }
-  o.KS = KS;
-  o.kpb = (o.nb + KS - 1) / KS;
-  // stages of a part: as few as fit, evened out
-  const int nst = (o.kpb + kcmax - 1) / kcmax;
-  o.KC = (o.kpb + nst - 1) / nst;
-  o.srb = seg_stride(o.type, o.KC);
-  // whole rows per stage: one copy per stage, rows at their memory stride
-  o.contig = (o.KS == 1 && o.KC == o.nb) ? 1 : 0;
-  if (o.contig) o.srb = static_cast<int32_t>(o.row_bytes);
-  o.ntiles = static_cast<int32_t>(ntiles);
-  o.nunits = static_cast<int32_t>(ntiles * KS);
+  set_split(o, KS, kcmax);
   return true;
 }
 
-// A contiguous stage adds 16 bytes of alignment and 16 of read slack (Q6_K's
-// unaligned reads); a per-row stage has both inside its row stride.
 int64_t stage_bytes(const KqOp& o) { return static_cast<int64_t>(8 * o.R) * o.srb + (o.contig ? 32 : 0); }
 
 struct LaunchGeom {
@@ -729,6 +748,59 @@ bool split_allowed(const ProgOpDesc* d, int n_ops, int i) {
   return true;
 }
 
+// K-parts of the ops of one stage (ops [i, j) between grid barriers): their
+// units are dealt to the CTAs round-robin, continuing from op to op, so the
+// parts are chosen together -- every combination of 1, 2, 4 or 8 parts per op
+// (where the op may split) is dealt out on the host and the one whose busiest
+// CTA has the fewest weight bytes (plus a fixed cost per unit) is kept.
+constexpr int64_t kUnitCost = 12288;  // bytes-equivalent of a unit's fixed work (waits, reduction)
+
+void balance_stage(const ProgOpDesc* d, int n_ops, KqOp* ops, int i, int j, int G) {
+  int cand[8][4], nc[8];
+  const int n = j - i;
+  if (n > 8) return;
+  int64_t combos = 1;
+  for (int k = 0; k < n; ++k) {
+    const KqOp& o = ops[i + k];
+    nc[k] = 0;
+    cand[k][nc[k]++] = 1;
+    if (split_allowed(d, n_ops, i + k))
+      for (int ks = 2; ks <= 8; ks *= 2)
+        if (split_ok(o.nb, ks)) cand[k][nc[k]++] = ks;
+    combos *= nc[k];
+  }
+  if (combos > 4096) return;
+  std::vector<int64_t> load(G);
+  int64_t best = -1;
+  int pick[8] = {0}, cur[8] = {0};
+  for (int64_t cmb = 0; cmb < combos; ++cmb) {
+    int64_t r = cmb;
+    for (int k = 0; k < n; ++k) { cur[k] = cand[k][r % nc[k]]; r /= nc[k]; }
+    std::fill(load.begin(), load.end(), 0);
+    int64_t rot = 0;
+    for (int k = 0; k < n; ++k) {
+      const KqOp& o = ops[i + k];
+      const int KS = cur[k], kpb = (o.nb + KS - 1) / KS, BB = block_bytes_of(o.type);
+      const int64_t units = static_cast<int64_t>(o.ntiles) * KS;
+      for (int64_t u = 0; u < units; ++u) {
+        const int kp = static_cast<int>(u % KS);
+        const int blocks = std::min(o.nb, (kp + 1) * kpb) - kp * kpb;
+        load[(u + rot) % G] += static_cast<int64_t>(8 * o.R) * blocks * BB + kUnitCost;
+      }
+      rot += units;
+    }
+    const int64_t mx = *std::max_element(load.begin(), load.end());
+    if (best < 0 || mx < best) {
+      best = mx;
+      for (int k = 0; k < n; ++k) pick[k] = cur[k];
+    }
+  }
+  for (int k = 0; k < n; ++k) {
+    KqOp& o = ops[i + k];
+    if (o.KS != pick[k]) set_split(o, pick[k], op_kcmax(o, kSlotCap));
+  }
+}
+
 // Plan every op of a program; false if some op cannot run on this path.
 // K is split only in programs with grid barriers (a program without them is
 // an ordinary launch that overlaps its neighbours and needs no final barrier).
@@ -747,9 +819,17 @@ bool plan_prog(const ProgOpDesc* descs, int n_ops, KqOp* ops, size_t* part_bytes
     o.type = descs[i].type;
     o.x_bf16 = descs[i].x_bf16;
     if (!plan_op(o, G, any_wait && split_allowed(descs, n_ops, i), kSlotCap)) return false;
-    if (o.KS > 1) pb += align256(static_cast<size_t>(o.ntiles) * o.KS * TT * sizeof(float));
     ops[i] = o;
   }
+  if (any_wait)
+    for (int i = 0; i < n_ops;) {
+      int j = i + 1;
+      while (j < n_ops && !descs[j].wait_previous) ++j;
+      balance_stage(descs, n_ops, ops, i, j, G);
+      i = j;
+    }
+  for (int i = 0; i < n_ops; ++i)
+    if (ops[i].KS > 1) pb += align256(static_cast<size_t>(ops[i].ntiles) * ops[i].KS * TT * sizeof(float));
   *part_bytes = pb;
   return true;
 }
