@@ -462,7 +462,8 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
   for (int oi = 0; oi < a.n_ops; ++oi) {
     const KqOp o = nxt;
     if (PROG && oi + 1 < a.n_ops) nxt = load_op<PROG>(a, oi + 1);
-    const int NL = o.x_bf16 ? 2 : 3;
+    // a program of one x dtype is compiled for it (NL0 = 2 or 3; 0: either)
+    const int NL = NL0 ? NL0 : (o.x_bf16 ? 2 : 3);
     if (oi > 0 && (o.flags & OP_WAIT)) {
       if constexpr (PROG) {
         for (; fixed < complete; ++fixed) {
@@ -855,7 +856,7 @@ cudaError_t prog_prepare(const ProgOpDesc* descs, int n_ops, void* ws, size_t ws
   if (ws_bytes < need) { delete[] ops; return cudaErrorInvalidValue; }
   uint8_t* w = static_cast<uint8_t*>(ws);
   size_t off = align256(kHeaderBytes + static_cast<size_t>(n_ops) * sizeof(KqOp));
-  int nb_max = 1, nl_max = 2, any_wait = 0, last_wait = 0, final_fix = 0;
+  int nb_max = 1, nl_max = 2, nl_min = 3, any_wait = 0, last_wait = 0, final_fix = 0;
   int64_t max_stage = 0, rot = 0;
   for (int i = 0; i < n_ops; ++i) {
     KqOp& o = ops[i];
@@ -872,6 +873,7 @@ cudaError_t prog_prepare(const ProgOpDesc* descs, int n_ops, void* ws, size_t ws
     }
     if (o.nb > nb_max) nb_max = o.nb;
     if (!o.x_bf16) nl_max = 3;
+    if (o.x_bf16) nl_min = 2;
     if (stage_bytes(o) > max_stage) max_stage = stage_bytes(o);
   }
   for (int i = last_wait; i < n_ops; ++i)
@@ -881,6 +883,7 @@ cudaError_t prog_prepare(const ProgOpDesc* descs, int n_ops, void* ws, size_t ws
   plan->n_ops = n_ops;
   plan->nb_max = nb_max;
   plan->nl_max = nl_max;
+  plan->nl_min = nl_min;
   plan->S = g.S;
   plan->slot = g.slot;
   plan->coop = (any_wait || final_fix) ? 1 : 0;
@@ -911,7 +914,11 @@ cudaError_t prog_run(const ProgPlan* plan, void* ws, cudaStream_t stream) {
   g.slot = plan->slot;
   g.smem = static_cast<size_t>(plan->smem);
   // grid barriers need every CTA resident: cooperative launch
-  return launch_prog<true, 0, 0, 4>(a, g, plan->coop != 0, stream, plan->coop == 0);
+  const bool coop = plan->coop != 0;
+  if (plan->nl_min == plan->nl_max)  // one x dtype: the kernel compiled for it only
+    return plan->nl_max == 2 ? launch_prog<true, 0, 2, 4>(a, g, coop, stream, !coop)
+                             : launch_prog<true, 0, 3, 4>(a, g, coop, stream, !coop);
+  return launch_prog<true, 0, 0, 4>(a, g, coop, stream, !coop);
 }
 
 }  // namespace kq

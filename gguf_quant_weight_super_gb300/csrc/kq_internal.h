@@ -45,7 +45,7 @@ struct ProgPlan {
   int n_ops, nb_max, nl_max, S, slot;
   int coop;       // grid barriers: cooperative launch
   int final_fix;  // split-K sums remain after the last op
-  int pad;
+  int nl_min;     // x limbs of the op with the fewest (equal to nl_max: one x dtype)
   int64_t smem, ws_bytes;
 };
 // workspace bytes of a program (0: some op cannot run on this path)

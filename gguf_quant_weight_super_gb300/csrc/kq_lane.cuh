@@ -123,13 +123,55 @@ __device__ __forceinline__ uint32_t pack_byte(int m0, int m1, int m2, int m3, in
   return __byte_perm(a, b, 0x5410);
 }
 
+// Writes oct o of the image from its integer values m[8] and the run's scale
+// (all lanes of the warp call it: the 16- and 32-run sums are shuffled).
+template <int NL>
+__device__ __forceinline__ void put_oct(const int (&m)[8], float scale, int o, int noct, const XImg& xi) {
+  int isum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) isum += m[j];
+  const int s16 = isum + __shfl_xor_sync(0xFFFFFFFFu, isum, 1);
+  const int s32 = s16 + __shfl_xor_sync(0xFFFFFFFFu, s16, 2);
+  if (o < noct) {
+    const int b = o >> 5, i = o & 31;
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+      const int k = NL - 1 - l;  // limb 0 = the most significant byte (signed)
+      const uint2 wv = make_uint2(pack_byte(m[0], m[1], m[2], m[3], k), pack_byte(m[4], m[5], m[6], m[7], k));
+      *reinterpret_cast<uint2*>(xi.limb + l * xi.plane + b * XWB + wpad_i(2 * i)) = wv;
+    }
+    if ((o & 15) == 0) xi.scale[o >> 4] = scale;
+    if ((o & 3) == 0) xi.si32[o >> 2] = s32;
+    if ((o & 1) == 0) {
+      const int r = (o >> 1) & 15;  // 16-run within the block
+      const int h = r >> 3, rr = r & 7;
+      xi.si16q[b * 16 + 4 * (2 * h + (rr & 1)) + (rr >> 1)] = s16;
+    }
+  }
+}
+
+// An oct whose 128-run maximum mx is zero, subnormal or huge (the exponent
+// taken with frexpf, the values scaled with ldexpf): out of line, rare.
+template <int NL>
+__device__ __noinline__ void stage_oct_slow(float v0, float v1, float v2, float v3, float v4, float v5, float v6,
+                                            float v7, float mx, int o, int noct, const XImg& xi) {
+  int e = 0;
+  frexpf(mx, &e);
+  const int shift = (NL == 2 ? 14 : 22) - e;
+  const float v[8] = {v0, v1, v2, v3, v4, v5, v6, v7};
+  int m[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m[j] = (mx > 0.0f) ? __float2int_rn(ldexpf(v[j], shift)) : 0;
+  put_oct<NL>(m, (mx > 0.0f) ? ldexpf(1.0f, -shift) : 0.0f, o, noct, xi);
+}
+
 // All consumer threads: quantize x[0..K) (zero past K up to nb*256) into xi.
 // Thread t takes "octs" (8 consecutive values) t, t+T, ...; the 32 octs of a
-// warp are one 256-block, 16 lanes one 128-run.  All global loads are issued
-// before any is used.
+// warp are one 256-block, 16 lanes one 128-run.  All global loads of a pass
+// (up to 6 octs a thread) are issued before any is used.
 template <int NL, int NTHR>
 __device__ void stage_x(const void* xp, int x_bf16, int K, int nb, const XImg& xi, int tid) {
-  constexpr int MAXO = 8;
+  constexpr int MAXO = 6;
   const int noct = nb * 32;
   const int lane = tid & 31;
   for (int base = 0; base < noct; base += MAXO * NTHR) {
@@ -163,45 +205,20 @@ __device__ void stage_x(const void* xp, int x_bf16, int K, int nb, const XImg& x
       for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(v[it][j]));
 #pragma unroll
       for (int w = 1; w < 16; w <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, w));
-      // mx = f * 2^e, f in [0.5, 1): from the bits for normal values, frexpf otherwise
+      // mx = f * 2^e, f in [0.5, 1): from the bits for normal values
       const uint32_t mb = __float_as_uint(mx);
       const int be = static_cast<int>((mb >> 23) & 0xFF);
-      const bool fast = be >= 40 && be <= 200;
-      int e = be - 126;
-      if (!fast) frexpf(mx, &e);
-      const int shift = (NL == 2 ? 14 : 22) - e;
+      if (__any_sync(0xFFFFFFFFu, be < 40 || be > 200)) {  // a run of this warp takes the slow path
+        stage_oct_slow<NL>(v[it][0], v[it][1], v[it][2], v[it][3], v[it][4], v[it][5], v[it][6], v[it][7], mx, o,
+                           noct, xi);
+        continue;
+      }
+      const int shift = (NL == 2 ? 14 : 22) - (be - 126);
+      const float p2 = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
       int m[8];
-      if (fast) {
-        const float p2 = __uint_as_float(static_cast<uint32_t>(127 + shift) << 23);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) m[j] = __float2int_rn(v[it][j] * p2);  // exact: power-of-two scale
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) m[j] = (mx > 0.0f) ? __float2int_rn(ldexpf(v[it][j], shift)) : 0;
-      }
-      int isum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) isum += m[j];
-      const int s16 = isum + __shfl_xor_sync(0xFFFFFFFFu, isum, 1);
-      const int s32 = s16 + __shfl_xor_sync(0xFFFFFFFFu, s16, 2);
-      if (o < noct) {
-        const int b = o >> 5, i = o & 31;
-#pragma unroll
-        for (int l = 0; l < NL; ++l) {
-          const int k = NL - 1 - l;  // limb 0 = the most significant byte (signed)
-          const uint2 wv = make_uint2(pack_byte(m[0], m[1], m[2], m[3], k), pack_byte(m[4], m[5], m[6], m[7], k));
-          *reinterpret_cast<uint2*>(xi.limb + l * xi.plane + b * XWB + wpad_i(2 * i)) = wv;
-        }
-        if ((o & 15) == 0)
-          xi.scale[o >> 4] = (mx > 0.0f) ? (fast ? __uint_as_float(static_cast<uint32_t>(127 - shift) << 23)
-                                                 : ldexpf(1.0f, -shift)) : 0.0f;
-        if ((o & 3) == 0) xi.si32[o >> 2] = s32;
-        if ((o & 1) == 0) {
-          const int r = (o >> 1) & 15;  // 16-run within the block
-          const int h = r >> 3, rr = r & 7;
-          xi.si16q[b * 16 + 4 * (2 * h + (rr & 1)) + (rr >> 1)] = s16;
-        }
-      }
+      for (int j = 0; j < 8; ++j) m[j] = __float2int_rn(v[it][j] * p2);  // exact: power-of-two scale
+      put_oct<NL>(m, __uint_as_float(static_cast<uint32_t>(127 - shift) << 23), o, noct, xi);
     }
   }
 }
