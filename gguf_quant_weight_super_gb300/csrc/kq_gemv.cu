@@ -100,7 +100,6 @@ struct ProgArgs {
   int nb_max, nl_max;
   int* barrier;      // grid barrier arrivals (programs with OP_WAIT), zero at launch
   int* err;
-  int pf;            // L2 prefetch distance in stages (0: none)
   int final_fix;     // split-K sums remain after the last op: final grid barrier
 };
 
@@ -358,30 +357,6 @@ __device__ __forceinline__ void cur_next(const ProgArgs& a, StageCursor& c, int 
   ++c.oi;
   cur_seek<PROG>(a, c, cta, G);
 }
-// L2 prefetch of a stage's row segments (lane i: row i; a contiguous stage:
-// lane 0, one prefetch).
-__device__ __forceinline__ void prefetch_stage(const StageCursor& c, int lane) {
-  const int BB = block_bytes_of(c.o.type);
-  if (c.o.contig) {
-    const int64_t r0 = static_cast<int64_t>(c.tile) * (8 * c.o.R);
-    if (lane == 0) {
-      const int64_t nrows = min_i64(8 * c.o.R, c.o.N - r0);
-      const uintptr_t s0 = reinterpret_cast<uintptr_t>(c.o.W + r0 * c.o.row_bytes);
-      const uintptr_t as = s0 & ~uintptr_t(15), ae = (s0 + nrows * c.o.row_bytes + 15) & ~uintptr_t(15);
-      bulk_prefetch_l2(reinterpret_cast<const void*>(as), static_cast<uint32_t>(ae - as));
-    }
-    return;
-  }
-  const int n = min(c.o.KC, c.kb1 - c.b0);
-  const int64_t row = static_cast<int64_t>(c.tile) * (8 * c.o.R) + lane;
-  if (lane < 8 * c.o.R && row < c.o.N) {
-    const uintptr_t s0 = reinterpret_cast<uintptr_t>(c.o.W + row * c.o.row_bytes + static_cast<int64_t>(c.b0) * BB);
-    const uintptr_t e0 = s0 + static_cast<uintptr_t>(n) * BB;
-    const uintptr_t as = s0 & ~uintptr_t(15), ae = (e0 + 15) & ~uintptr_t(15);
-    bulk_prefetch_l2(reinterpret_cast<const void*>(as), static_cast<uint32_t>(ae - as));
-  }
-}
-
 // Shared memory: barriers and counters (256 B), the ring, the reduction
 // buffers, the x image.
 __host__ __device__ inline size_t red_bytes(int S) { return static_cast<size_t>(S + 1) * NC * TT * 4; }
@@ -419,18 +394,12 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
     pdl_launch_dependents();
     int q = 0, slot = 0;
     uint32_t lap = 0;  // parity of the ring lap
-    StageCursor cc, pc;
+    StageCursor cc;
     cur_start<PROG>(a, cc, cta, G);
-    pc = cc;
-    for (int k = 0; k < a.pf && pc.valid; ++k) cur_next<PROG>(a, pc, cta, G);
     while (cc.valid) {
       if (q >= a.S) {  // the slot's previous stage has been consumed
         const bool ok = mbar_wait(&rg.empty[slot], lap ^ 1u, a.err);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      }
-      if (a.pf > 0 && pc.valid) {  // ask L2 for the stage a.pf stages ahead
-        prefetch_stage(pc, lane);
-        cur_next<PROG>(a, pc, cta, G);
       }
       produce(cc.o, cc.tile, cc.b0, min(cc.o.KC, cc.kb1 - cc.b0), rg.base + static_cast<size_t>(slot) * a.slot,
               &rg.full[slot], lane, block_bytes_of(cc.o.type));
@@ -464,7 +433,7 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
     if (PROG && oi + 1 < a.n_ops) nxt = load_op<PROG>(a, oi + 1);
     // a program of one x dtype is compiled for it (NL0 = 2 or 3; 0: either)
     const int NL = NL0 ? NL0 : (o.x_bf16 ? 2 : 3);
-    if (oi > 0 && (o.flags & OP_WAIT)) {
+    if (PROG && oi > 0 && (o.flags & OP_WAIT)) {
       if constexpr (PROG) {
         for (; fixed < complete; ++fixed) {
           const KqOp f = load_op<PROG>(a, fixed);
@@ -504,7 +473,7 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
       if (f.KS > 1) fixup_op(f, cta, G, ctid);
     }
   }
-  if (a.barrier) {
+  if (PROG && a.barrier) {
     // final barrier (only when split-K sums of the last stage remain), then
     // the exit count: the last CTA to leave resets both counters for the next
     // launch
@@ -681,7 +650,6 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 }  // namespace
 
 namespace {
-int g_prefetch_stages = 0;  // L2 prefetch distance (stages beyond the one being copied; 0: none)
 
 template <int QT, int NL>
 cudaError_t launch_single_r(int R, ProgArgs& a, const LaunchGeom& g, cudaStream_t st, bool pdl) {
@@ -705,7 +673,6 @@ cudaError_t launch_single(int qtype, int NL, int R, ProgArgs& a, const LaunchGeo
   }
 }
 }  // namespace
-void set_prefetch_stages(int pf) { g_prefetch_stages = pf < 0 ? 0 : pf; }
 
 cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, float* y, int64_t N, int K,
                            cudaStream_t stream, bool pdl) {
@@ -729,7 +696,6 @@ cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, 
   a.nl_max = x_bf16 ? 2 : 3;
   a.barrier = nullptr;
   a.err = device_error_ptr();
-  a.pf = g_prefetch_stages;
   return launch_single(qtype, x_bf16 ? 2 : 3, o.R, a, g, stream, pdl);
 }
 
@@ -908,7 +874,6 @@ cudaError_t prog_run(const ProgPlan* plan, void* ws, cudaStream_t stream) {
   a.barrier = plan->coop ? static_cast<int*>(ws) : nullptr;
   a.final_fix = plan->final_fix;
   a.err = device_error_ptr();
-  a.pf = g_prefetch_stages;
   LaunchGeom g;
   g.S = plan->S;
   g.slot = plan->slot;

@@ -54,8 +54,6 @@ size_t prog_workspace_size(const ProgOpDesc* descs, int n_ops);
 cudaError_t prog_prepare(const ProgOpDesc* descs, int n_ops, void* ws, size_t ws_bytes, ProgPlan* plan,
                          cudaStream_t stream);
 cudaError_t prog_run(const ProgPlan* plan, void* ws, cudaStream_t stream);
-// L2 prefetch distance of the one-token kernel, in stages (0: none)
-void set_prefetch_stages(int pf);
 
 // M = 2..16 tokens, bf16 x, on the tensor cores (kq_tc.cu)
 bool tc_supported(int qtype, int64_t N, int K, int M);
