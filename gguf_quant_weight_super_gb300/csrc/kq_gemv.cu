@@ -56,9 +56,9 @@ using namespace lane;
 namespace {
 
 #ifndef KQ_NC
-#define KQ_NC 7
+#define KQ_NC 11
 #endif
-constexpr int NC = KQ_NC;              // consumer warps (+1 producer: 8 warps, all registers usable)
+constexpr int NC = KQ_NC;              // consumer warps (+1 producer: 12 warps, three warpgroups, 170 registers a thread)
 constexpr int TT = 32;                 // rows per tile (4 per quad)
 constexpr int NTHC = NC * 32;          // consumer threads
 constexpr int NTH = NTHC + 32;         // + one producer warp
