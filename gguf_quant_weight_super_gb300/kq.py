@@ -43,12 +43,24 @@ SIGNATURES = {
 }
 
 
-def build_id() -> str:
-    """Hash of the kernel sources (identifies which code a profile was taken on)."""
+# The sources each kernel family is compiled from (the one-token / program
+# kernel: kq_gemv.cu and the headers it includes).
+KERNEL_SOURCES = {
+    "prog_kernel": ("kq_gemv.cu", "kq_lane.cuh", "kq_ptx.cuh", "kq_internal.h", "kq_decode.cuh"),
+}
+
+
+def build_id(kernel=None) -> str:
+    """Hash of the kernel sources (identifies which code a profile was taken
+    on): all of csrc, or only the files of one kernel family."""
     import glob
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(PKG, "csrc", "*"))):
+    if kernel is None:
+        files = sorted(glob.glob(os.path.join(PKG, "csrc", "*")))
+    else:
+        files = [os.path.join(PKG, "csrc", n) for n in KERNEL_SOURCES[kernel]]
+    for f in files:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
             h.update(fh.read())
