@@ -479,7 +479,7 @@ def main():
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             tr = json.load(f)
-        if tr.get("kernel_build") == kq.build_id("prog_kernel") and tr.get("variant") == best:
+        if tr.get("kernel_build") == kq.build_id("prog_kernel") and best in tr.get("variants", []):
             # DRAM bytes per launch from one ncu capture (ratio to the weight
             # bytes), scaled to the average launch of this variant
             traffic = tr["dram_bytes_ratio"] * q4_bytes / n_q4
