@@ -32,14 +32,15 @@
 //    full with 1-D TMA bulk copies: one copy per stage when a stage holds
 //    whole rows, else one copy per row segment of KC blocks.  Weights never
 //    depend on earlier ops, so the producer runs ahead across op boundaries;
-//  * consumer warp w owns rows w*TT/8 .. of a tile; quad q of the warp takes
-//    one of those rows and one block phase (block b0+ph, b0+ph+P, ...), so a
-//    stage of TT rows x KC blocks keeps all 64 quads busy whenever KC is a
-//    multiple of P = 64/TT; row sums reduce over fixed shuffle trees
-//    (deterministic);
-//  * a tile whose K is split across CTAs writes its partial row sums to the
-//    workspace; the last CTA to finish the tile (arrival counter) adds them in
-//    part order and writes y;
+//  * a stage's blocks are dealt to the consumer warps round-robin (continuing
+//    across stages); quad q of a warp owns the tile rows q, q+8, ... (R of
+//    them: a tile is 8R rows), so one x slice, loaded once per block, serves
+//    R rows; a unit's row sums are added over the quad's lanes by shuffles and
+//    over the warps in warp order by the unit's last warp (deterministic);
+//  * in a program with grid barriers a tile's K may be split across CTAs: the
+//    parts' row sums go to the workspace and are added in part order, each CTA
+//    for its slice of rows, before the barrier that follows the one after
+//    which they are complete (or after a final barrier);
 //  * an op flagged "wait for previous" starts with a grid barrier (all CTAs
 //    resident: cooperative launch) before its x is read; single products
 //    instead use programmatic dependent launch, streaming weights before
