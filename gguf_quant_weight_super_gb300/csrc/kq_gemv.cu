@@ -66,6 +66,7 @@ constexpr int NTH = NTHC + 32;         // + one producer warp
 constexpr int RING_MAX = 8;                // ring slots at most
 constexpr int CONSUMER_BAR = 1;        // named barrier of the consumer warps
 constexpr int MAX_NB = 64;             // K <= 16384
+constexpr int kMaxTokens1 = 2;         // tokens of one single-product launch (bf16 x when more than one)
 // Largest stage (32 row segments): 48 KB keeps a ring of at least 4 slots.
 constexpr int64_t kSlotCap = 48 * 1024;
 // Largest stage of whole rows (one bulk copy), by rows per quad: a taller
@@ -195,10 +196,13 @@ struct Walk {
 // Consumers: every unit of op o for this CTA.  Quad q of every warp owns the
 // tile rows q, q+8, ... (R of them; a tile is 8R rows); the stage's blocks
 // are dealt to the warps round-robin (continuing across stages), so a warp
-// applies one x slice to the R rows of each of its 8 quads.
-template <int QT, int NL, int R>
-__device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const Red& rd, Walk& wk, int* err,
+// applies one x slice to the R rows of each of its 8 quads.  With MT > 1
+// tokens (single products) the block is unpacked once per row and dotted
+// with every token's slice; y is [MT][N].
+template <int QT, int NL, int R, int MT = 1>
+__device__ void consume_op(const KqOp& o, const XImg (&xs)[MT], const Ring& rg, const Red& rd, Walk& wk, int* err,
                            int cta, int G) {
+  const XImg& xi = xs[0];
   constexpr int BB = Fmt<QT>::BYTES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = lane >> 2, c = lane & 3;
@@ -209,9 +213,11 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
     const int kb0 = kp * o.kpb;
     const int kb1 = min(o.nb, kb0 + o.kpb);
     const int64_t row0 = static_cast<int64_t>(tile) * (8 * R);
-    float acc[R];
+    float acc[R][MT];
 #pragma unroll
-    for (int i = 0; i < R; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+      for (int t = 0; t < MT; ++t) acc[i][t] = 0.0f;
     for (int b0 = kb0; b0 < kb1; b0 += o.KC) {
       const int n = min(o.KC, kb1 - b0);
       const int slot = wk.slot;
@@ -238,20 +244,50 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
         }
         for (; bi < n; bi += NC) {
           const int b = b0 + bi;
-          XSlice<NL> X;
-          load_slice<QT, NL>(xi.limb_s + 4 * (b * XWB + xoff), 4 * xi.plane, X);
-          const float s = __uint_as_float(lds32(xi.scale_s + 4 * (2 * b + (c >> 1))));
-          if constexpr (QT == T_Q6_K) {
-            const uint4 sv = lds128(xi.si16q_s + 4 * (16 * b + 4 * c));
-            const int4 si = make_int4(static_cast<int>(sv.x), static_cast<int>(sv.y), static_cast<int>(sv.z),
-                                      static_cast<int>(sv.w));
+          if constexpr (MT == 1) {
+            XSlice<NL> X;
+            load_slice<QT, NL>(xi.limb_s + 4 * (b * XWB + xoff), 4 * xi.plane, X);
+            const float s = __uint_as_float(lds32(xi.scale_s + 4 * (2 * b + (c >> 1))));
+            if constexpr (QT == T_Q6_K) {
+              const uint4 sv = lds128(xi.si16q_s + 4 * (16 * b + 4 * c));
+              const int4 si = make_int4(static_cast<int>(sv.x), static_cast<int>(sv.y), static_cast<int>(sv.z),
+                                        static_cast<int>(sv.w));
 #pragma unroll
-            for (int i = 0; i < R; ++i) acc[i] = core_q6<NL>(rp[i], X, si, s, c, acc[i]);
+              for (int i = 0; i < R; ++i) acc[i][0] = core_q6<NL>(rp[i], X, si, s, c, acc[i][0]);
+            } else {
+              const uint2 sv = lds64(xi.si32_s + 4 * (8 * b + 2 * c));
+              const int2 si = make_int2(static_cast<int>(sv.x), static_cast<int>(sv.y));
+#pragma unroll
+              for (int i = 0; i < R; ++i) acc[i][0] = core_q45<QT, NL>(rp[i], X, si, s, c, sl, acc[i][0]);
+            }
           } else {
-            const uint2 sv = lds64(xi.si32_s + 4 * (8 * b + 2 * c));
-            const int2 si = make_int2(static_cast<int>(sv.x), static_cast<int>(sv.y));
+            XSlice<NL> X[MT];
+            float s[MT];
 #pragma unroll
-            for (int i = 0; i < R; ++i) acc[i] = core_q45<QT, NL>(rp[i], X, si, s, c, sl, acc[i]);
+            for (int t = 0; t < MT; ++t) {
+              load_slice<QT, NL>(xs[t].limb_s + 4 * (b * XWB + xoff), 4 * xs[t].plane, X[t]);
+              s[t] = __uint_as_float(lds32(xs[t].scale_s + 4 * (2 * b + (c >> 1))));
+            }
+            if constexpr (QT == T_Q6_K) {
+              int4 si[MT];
+#pragma unroll
+              for (int t = 0; t < MT; ++t) {
+                const uint4 sv = lds128(xs[t].si16q_s + 4 * (16 * b + 4 * c));
+                si[t] = make_int4(static_cast<int>(sv.x), static_cast<int>(sv.y), static_cast<int>(sv.z),
+                                  static_cast<int>(sv.w));
+              }
+#pragma unroll
+              for (int i = 0; i < R; ++i) core_q6_mt<NL, MT>(rp[i], X, si, s, c, acc[i]);
+            } else {
+              int2 si[MT];
+#pragma unroll
+              for (int t = 0; t < MT; ++t) {
+                const uint2 sv = lds64(xs[t].si32_s + 4 * (8 * b + 2 * c));
+                si[t] = make_int2(static_cast<int>(sv.x), static_cast<int>(sv.y));
+              }
+#pragma unroll
+              for (int i = 0; i < R; ++i) core_q45_mt<QT, NL, MT>(rp[i], X, si, s, c, sl, acc[i]);
+            }
           }
 #pragma unroll
           for (int i = 0; i < R; ++i) rp[i] += NC * BB;
@@ -264,16 +300,20 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
     }
     // this warp's partial row sums: over the quad's lanes, then to shared memory
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xFFFFFFFFu, acc[i], 1));
-      acc[i] = __fadd_rn(acc[i], __shfl_xor_sync(0xFFFFFFFFu, acc[i], 2));
-    }
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        acc[i][t] = __fadd_rn(acc[i][t], __shfl_xor_sync(0xFFFFFFFFu, acc[i][t], 1));
+        acc[i][t] = __fadd_rn(acc[i][t], __shfl_xor_sync(0xFFFFFFFFu, acc[i][t], 2));
+      }
     const int rs = wk.rs;
     if (++wk.rs == rd.RS) wk.rs = 0;
-    float* rb = rd.buf + static_cast<size_t>(rs) * NC * TT;
+    float* rb = rd.buf + static_cast<size_t>(rs) * NC * TT * MT;  // [MT][NC][TT]
     if (c == 0) {
 #pragma unroll
-      for (int i = 0; i < R; ++i) rb[warp * TT + quad + 8 * i] = acc[i];
+      for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) rb[(t * NC + warp) * TT + quad + 8 * i] = acc[i][t];
     }
     __syncwarp();
     int last = 0;
@@ -285,15 +325,23 @@ __device__ void consume_op(const KqOp& o, const XImg& xi, const Ring& rg, const 
     if (!last) continue;
     // last warp of the unit: add the warps' partials in warp order
     __threadfence_block();
-    float v = rb[lane];
+    float v[MT];
 #pragma unroll
-    for (int w = 1; w < NC; ++w) v = __fadd_rn(v, rb[w * TT + lane]);
+    for (int t = 0; t < MT; ++t) {
+      v[t] = rb[t * NC * TT + lane];
+#pragma unroll
+      for (int w = 1; w < NC; ++w) v[t] = __fadd_rn(v[t], rb[(t * NC + w) * TT + lane]);
+    }
     __syncwarp();
     if (lane == 0) rd.cnt[rs] = 0;
     const int64_t row = row0 + lane;
     if (lane < 8 * R && row < o.N && !wk.failed) {
-      if (o.KS == 1) o.y[row] = v;
-      else o.part[static_cast<int64_t>(kp) * o.ntiles * TT + row] = v;  // added at the next grid barrier
+      if (o.KS == 1) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t) o.y[t * o.N + row] = v[t];
+      } else {
+        o.part[static_cast<int64_t>(kp) * o.ntiles * TT + row] = v[0];  // added at the next grid barrier
+      }
     }
   }
 }
@@ -312,9 +360,10 @@ __device__ __forceinline__ void fixup_op(const KqOp& o, int cta, int G, int ctid
 template <int NL>
 __device__ __forceinline__ void consume_any(const KqOp& o, const XImg& xi, const Ring& rg, const Red& rd, Walk& wk,
                                             int* err, int cta, int G) {
-  if (o.type == T_Q4_K) consume_op<T_Q4_K, NL, 4>(o, xi, rg, rd, wk, err, cta, G);
-  else if (o.type == T_Q5_K) consume_op<T_Q5_K, NL, 4>(o, xi, rg, rd, wk, err, cta, G);
-  else consume_op<T_Q6_K, NL, 4>(o, xi, rg, rd, wk, err, cta, G);
+  const XImg xs[1] = {xi};
+  if (o.type == T_Q4_K) consume_op<T_Q4_K, NL, 4>(o, xs, rg, rd, wk, err, cta, G);
+  else if (o.type == T_Q5_K) consume_op<T_Q5_K, NL, 4>(o, xs, rg, rd, wk, err, cta, G);
+  else consume_op<T_Q6_K, NL, 4>(o, xs, rg, rd, wk, err, cta, G);
 }
 
 template <bool PROG>
@@ -360,12 +409,14 @@ __device__ __forceinline__ void cur_next(const ProgArgs& a, StageCursor& c, int 
 }
 // Shared memory: barriers and counters (256 B), the ring, the reduction
 // buffers, the x image.
-__host__ __device__ inline size_t red_bytes(int S) { return static_cast<size_t>(S + 1) * NC * TT * 4; }
+__host__ __device__ inline size_t red_bytes(int S, int mt = 1) { return static_cast<size_t>(S + 1) * NC * TT * 4 * mt; }
+// x images of a launch: one per token, 16-byte aligned
+__host__ __device__ inline size_t ximg_stride(int nb, int nl) { return (ximg_bytes(nb, nl) + 15) & ~size_t(15); }
 
 // PROG: ops in global memory (any types); else the single op a.op0, whose
 // type and x limb count are the template's QT0 and NL0 (one instantiation per
 // format and x dtype keeps the single-product code small).
-template <bool PROG, int QT0, int NL0, int R0>
+template <bool PROG, int QT0, int NL0, int R0, int MT0 = 1>
 __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ ProgArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   Ring rg;
@@ -379,7 +430,7 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
   rd.cnt = reinterpret_cast<int*>(rg.empty + RING_MAX);  // RING_MAX + 1 ints
   rd.RS = a.S + 1;
   rd.buf = reinterpret_cast<float*>(rg.base + static_cast<size_t>(a.S) * a.slot);
-  uint8_t* xbase = reinterpret_cast<uint8_t*>(rd.buf) + red_bytes(a.S);
+  uint8_t* xbase = reinterpret_cast<uint8_t*>(rd.buf) + red_bytes(a.S, MT0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
 
@@ -453,10 +504,17 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
     }
     const XImg xi = ximg_at(xbase, a.nb_max, a.nl_max);
     if constexpr (!PROG) {
+      // one x image per token (x is [MT0][K])
+      XImg xs[MT0];
       consumer_sync();
-      stage_x<NL0, NTHC>(o.x, NL0 == 2, o.K, o.nb, xi, ctid);
+#pragma unroll
+      for (int t = 0; t < MT0; ++t) {
+        xs[t] = ximg_at(xbase + t * ximg_stride(a.nb_max, a.nl_max), a.nb_max, a.nl_max);
+        const void* xt = static_cast<const uint8_t*>(o.x) + static_cast<size_t>(t) * o.K * (NL0 == 2 ? 2 : 4);
+        stage_x<NL0, NTHC>(xt, NL0 == 2, o.K, o.nb, xs[t], ctid);
+      }
       consumer_sync();
-      consume_op<QT0, NL0, R0>(o, xi, rg, rd, wk, a.err, cta, G);
+      consume_op<QT0, NL0, R0, MT0>(o, xs, rg, rd, wk, a.err, cta, G);
       continue;
     }
     if (oi == 0 || (o.flags & (OP_NEWX | OP_WAIT))) {
@@ -598,25 +656,26 @@ struct LaunchGeom {
   size_t smem;
 };
 
-bool ring_geom(int64_t max_stage, int nb_max, int nl_max, LaunchGeom& g) {
+bool ring_geom(int64_t max_stage, int nb_max, int nl_max, LaunchGeom& g, int mt = 1) {
   g.slot = static_cast<int>((max_stage + 127) & ~int64_t(127));
-  const size_t fixed = 256 + ximg_bytes(nb_max, nl_max);
+  const size_t fixed = 256 + mt * ximg_stride(nb_max, nl_max);
   int S = RING_MAX;
-  while (S >= 2 && fixed + static_cast<size_t>(S) * g.slot + red_bytes(S) > static_cast<size_t>(kMaxSmemPerBlock)) --S;
+  while (S >= 2 && fixed + static_cast<size_t>(S) * g.slot + red_bytes(S, mt) > static_cast<size_t>(kMaxSmemPerBlock))
+    --S;
   if (S < 2) return false;
   g.S = S;
-  g.smem = fixed + static_cast<size_t>(S) * g.slot + red_bytes(S);
+  g.smem = fixed + static_cast<size_t>(S) * g.slot + red_bytes(S, mt);
   return true;
 }
 
-template <bool PROG, int QT0, int NL0, int R0>
+template <bool PROG, int QT0, int NL0, int R0, int MT0 = 1>
 cudaError_t launch_prog(ProgArgs& a, const LaunchGeom& g, bool cooperative, cudaStream_t st, bool pdl) {
   a.S = g.S;
   a.slot = g.slot;
   static bool smem_set[64] = {false};
   const int dev = current_device_id();
   if (!smem_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prog_kernel<PROG, QT0, NL0, R0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prog_kernel<PROG, QT0, NL0, R0, MT0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kMaxSmemPerBlock);
     if (e != cudaSuccess) return e;
     smem_set[dev] = true;
@@ -640,7 +699,7 @@ cudaError_t launch_prog(ProgArgs& a, const LaunchGeom& g, bool cooperative, cuda
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, prog_kernel<PROG, QT0, NL0, R0>, a);
+  return cudaLaunchKernelEx(&cfg, prog_kernel<PROG, QT0, NL0, R0, MT0>, a);
 }
 
 // Program workspace: header (grid barrier counter), ops, split-K partials and counters.
@@ -652,12 +711,12 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 namespace {
 
-template <int QT, int NL>
+template <int QT, int NL, int MT = 1>
 cudaError_t launch_single_r(int R, ProgArgs& a, const LaunchGeom& g, cudaStream_t st, bool pdl) {
   switch (R) {
-    case 4: return launch_prog<false, QT, NL, 4>(a, g, false, st, pdl);
-    case 2: return launch_prog<false, QT, NL, 2>(a, g, false, st, pdl);
-    case 1: return launch_prog<false, QT, NL, 1>(a, g, false, st, pdl);
+    case 4: return launch_prog<false, QT, NL, 4, MT>(a, g, false, st, pdl);
+    case 2: return launch_prog<false, QT, NL, 2, MT>(a, g, false, st, pdl);
+    case 1: return launch_prog<false, QT, NL, 1, MT>(a, g, false, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -676,8 +735,9 @@ cudaError_t launch_single(int qtype, int NL, int R, ProgArgs& a, const LaunchGeo
 }  // namespace
 
 cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, float* y, int64_t N, int K,
-                           cudaStream_t stream, bool pdl) {
+                           cudaStream_t stream, bool pdl, int M) {
   if (N == 0) return cudaSuccess;
+  if (M < 1 || M > kMaxTokens1 || (M > 1 && !x_bf16)) return cudaErrorNotSupported;
   ProgArgs a = {};
   KqOp& o = a.op0;
   o.W = static_cast<const uint8_t*>(W);
@@ -690,13 +750,21 @@ cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, 
   o.flags = OP_NEWX;
   if (!plan_op(o, num_sms(), false, kSlotCap, true)) return cudaErrorNotSupported;
   LaunchGeom g;
-  if (!ring_geom(stage_bytes(o), o.nb, x_bf16 ? 2 : 3, g)) return cudaErrorNotSupported;
+  if (!ring_geom(stage_bytes(o), o.nb, x_bf16 ? 2 : 3, g, M)) return cudaErrorNotSupported;
   a.ops = nullptr;
   a.n_ops = 1;
   a.nb_max = o.nb;
   a.nl_max = x_bf16 ? 2 : 3;
   a.barrier = nullptr;
   a.err = device_error_ptr();
+  if (M == 2) {  // two tokens: bf16 x only (the x slices of both tokens stay in registers)
+    switch (qtype) {
+      case T_Q4_K: return launch_single_r<T_Q4_K, 2, 2>(o.R, a, g, stream, pdl);
+      case T_Q5_K: return launch_single_r<T_Q5_K, 2, 2>(o.R, a, g, stream, pdl);
+      case T_Q6_K: return launch_single_r<T_Q6_K, 2, 2>(o.R, a, g, stream, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   return launch_single(qtype, x_bf16 ? 2 : 3, o.R, a, g, stream, pdl);
 }
 

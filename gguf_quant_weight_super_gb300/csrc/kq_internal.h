@@ -32,8 +32,9 @@ cudaError_t launch_gemv1(int qtype, const void* W, const void* x, int x_bf16, fl
 // One-token products (kq_gemv.cu): a single product, or a program of
 // products run by one persistent launch with grid-wide ordering between
 // dependent ones and split-K partial sums in the program's workspace.
+// (M tokens: 1, or 2 with bf16 x; y is [M][N])
 cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, float* y, int64_t N, int K,
-                           cudaStream_t stream, bool pdl);
+                           cudaStream_t stream, bool pdl, int M = 1);
 struct ProgOpDesc {
   int type, x_bf16, wait_previous;
   const void* W;

@@ -392,5 +392,147 @@ __device__ __forceinline__ float core_q6(uint32_t bp, const XSlice<NL>& X, int4 
 }
 
 
+// ----------------------------------------------- several tokens per block
+// The same lane arithmetic for MT tokens: the block's bytes are read and its
+// codes and scales unpacked once, then dotted with every token's x slice.
+
+// Q4_K / Q5_K (see core_q45): acc[t] += this lane's part of token t's row sum.
+template <int QT, int NL, int MT>
+__device__ __forceinline__ void core_q45_mt(uint32_t bp, const XSlice<NL> (&X)[MT], const int2 (&si)[MT],
+                                            const float (&s)[MT], int c, const ScaleLane& sl, float (&acc)[MT]) {
+  const uint4 hdr = lds128(bp);
+  constexpr int QS = (QT == T_Q4_K) ? 16 : 48;
+  const uint4 q0 = lds128(bp + QS + 32 * c);
+  const uint4 q1 = lds128(bp + QS + 32 * c + 16);
+  uint4 h0 = make_uint4(0, 0, 0, 0), h1 = make_uint4(0, 0, 0, 0);
+  if constexpr (QT == T_Q5_K) { h0 = lds128(bp + 16); h1 = lds128(bp + 32); }
+  int I[MT][2][NL];
+#pragma unroll
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+      for (int l = 0; l < NL; ++l) I[t][p][l] = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t q = (w < 4) ? w4(q0, w) : w4(q1, w - 4);
+    uint32_t lo, hi;
+    if constexpr (QT == T_Q4_K) {
+      lo = q & 0x0F0F0F0Fu;
+      hi = q & 0xF0F0F0F0u;  // 16 x the high nibble: the factor leaves T_1 exactly
+    } else {
+      const uint32_t hb = (w < 4) ? w4(h0, w) : w4(h1, w - 4);
+      lo = (q & 0x0F0F0F0Fu) | (__funnelshift_l(hb, hb, (4 - 2 * c) & 31) & 0x10101010u);
+      hi = ((q >> 4) & 0x0F0F0F0Fu) | (__funnelshift_l(hb, hb, (3 - 2 * c) & 31) & 0x10101010u);
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      I[t][0][0] = dp_us(lo, X[t].w[0][w], I[t][0][0]);
+      I[t][1][0] = dp_us(hi, X[t].w[0][8 + w], I[t][1][0]);
+#pragma unroll
+      for (int l = 1; l < NL; ++l) {
+        I[t][0][l] = dp_uu(lo, X[t].w[l][w], I[t][0][l]);
+        I[t][1][l] = dp_uu(hi, X[t].w[l][8 + w], I[t][1][l]);
+      }
+    }
+  }
+  const uint32_t P = __byte_perm(sl.lowsrc ? hdr.y : hdr.w, hdr.z, sl.selP);
+  const uint32_t Q = __byte_perm(hdr.y, hdr.z, sl.selQ);
+  const uint32_t L = (P & sl.mA) | ((P >> 4) & sl.mB) | ((Q >> 2) & sl.mH);
+  const int sc0 = static_cast<int>(L & 0xFF), sc1 = static_cast<int>((L >> 8) & 0xFF);
+  const int m0 = static_cast<int>((L >> 16) & 0xFF), m1 = static_cast<int>(L >> 24);
+  const float d = half_bits_to_float(hdr.x & 0xFFFF);
+  const float dmin = half_bits_to_float(hdr.x >> 16);
+#pragma unroll
+  for (int t = 0; t < MT; ++t) {
+    if constexpr (NL == 2) {
+      const int T0 = I[t][0][0] * 256 + I[t][0][1];
+      int T1 = I[t][1][0] * 256 + I[t][1][1];
+      if constexpr (QT == T_Q4_K) T1 >>= 4;
+      const int Y = sc0 * T0 + sc1 * T1;
+      const int Mi = m0 * si[t].x + m1 * si[t].y;
+      acc[t] = __fmaf_rn(s[t], __fmaf_rn(d, static_cast<float>(Y), -dmin * static_cast<float>(Mi)), acc[t]);
+    } else {
+      int Yl[NL];
+#pragma unroll
+      for (int l = 0; l < NL; ++l) {
+        int t1 = I[t][1][l];
+        if constexpr (QT == T_Q4_K) t1 >>= 4;
+        Yl[l] = sc0 * I[t][0][l] + sc1 * t1;
+      }
+      const float Yf = __fmaf_rn(static_cast<float>(Yl[0]), 65536.0f,
+                                 __fmaf_rn(static_cast<float>(Yl[1]), 256.0f, static_cast<float>(Yl[2])));
+      const float Mf = __fmaf_rn(static_cast<float>(m0), static_cast<float>(si[t].x),
+                                 static_cast<float>(m1) * static_cast<float>(si[t].y));
+      acc[t] = __fmaf_rn(s[t], __fmaf_rn(d, Yf, -dmin * Mf), acc[t]);
+    }
+  }
+}
+
+// Q6_K (see core_q6), MT tokens.
+template <int NL, int MT>
+__device__ __forceinline__ void core_q6_mt(uint32_t bp, const XSlice<NL> (&X)[MT], const int4 (&si)[MT],
+                                           const float (&s)[MT], int c, float (&acc)[MT]) {
+  const int h = c >> 1, e = c & 1;
+  const uint4 qa = lds16_a2(bp + 64 * h + 16 * e);
+  const uint4 qb = lds16_a2(bp + 64 * h + 32 + 16 * e);
+  const uint4 qh = lds16_a2(bp + 128 + 32 * h + 16 * e);
+  const uint2 sv = lds8_a2(bp + 192 + 8 * h);
+  const uint32_t se = __byte_perm(sv.x, sv.y, e ? 0x7531 : 0x6420);  // scales 8h + 2p + e, p = 0..3
+  const float d = half_bits_to_float(lds16(bp + 208));
+  int I[MT][4][NL];
+#pragma unroll
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+      for (int l = 0; l < NL; ++l) I[t][p][l] = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t a = w4(qa, w), b = w4(qb, w), hv = w4(qh, w);
+    uint32_t cd[4];
+    cd[0] = (a & 0x0F0F0F0Fu) | ((hv << 4) & 0x30303030u);
+    cd[1] = (b & 0x0F0F0F0Fu) | ((hv << 2) & 0x30303030u);
+    cd[2] = ((a >> 4) & 0x0F0F0F0Fu) | (hv & 0x30303030u);
+    cd[3] = ((b >> 4) & 0x0F0F0F0Fu) | ((hv >> 2) & 0x30303030u);
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        I[t][p][0] = dp_us(cd[p], X[t].w[0][4 * p + w], I[t][p][0]);
+#pragma unroll
+        for (int l = 1; l < NL; ++l) I[t][p][l] = dp_uu(cd[p], X[t].w[l][4 * p + w], I[t][p][l]);
+      }
+  }
+  const int sc0 = sbyte(se, 0), sc1 = sbyte(se, 1), sc2 = sbyte(se, 2), sc3 = sbyte(se, 3);
+#pragma unroll
+  for (int t = 0; t < MT; ++t) {
+    const float sd = s[t] * d;
+    if constexpr (NL == 2) {
+      const int T0 = I[t][0][0] * 256 + I[t][0][1] - 32 * si[t].x;
+      const int T1 = I[t][1][0] * 256 + I[t][1][1] - 32 * si[t].y;
+      const int T2 = I[t][2][0] * 256 + I[t][2][1] - 32 * si[t].z;
+      const int T3 = I[t][3][0] * 256 + I[t][3][1] - 32 * si[t].w;
+      const int Ya = sc0 * T0 + sc1 * T1;
+      const int Yb = sc2 * T2 + sc3 * T3;
+      acc[t] = __fmaf_rn(sd, static_cast<float>(Ya), acc[t]);
+      acc[t] = __fmaf_rn(sd, static_cast<float>(Yb), acc[t]);
+    } else {
+      int Yl[NL];
+#pragma unroll
+      for (int l = 0; l < NL; ++l)
+        Yl[l] = sc0 * I[t][0][l] + sc1 * I[t][1][l] + sc2 * I[t][2][l] + sc3 * I[t][3][l];
+      const float Yf = __fmaf_rn(static_cast<float>(Yl[0]), 65536.0f,
+                                 __fmaf_rn(static_cast<float>(Yl[1]), 256.0f, static_cast<float>(Yl[2])));
+      float Z = static_cast<float>(sc0) * static_cast<float>(si[t].x);
+      Z = __fmaf_rn(static_cast<float>(sc1), static_cast<float>(si[t].y), Z);
+      Z = __fmaf_rn(static_cast<float>(sc2), static_cast<float>(si[t].z), Z);
+      Z = __fmaf_rn(static_cast<float>(sc3), static_cast<float>(si[t].w), Z);
+      acc[t] = __fmaf_rn(sd, __fmaf_rn(-32.0f, Z, Yf), acc[t]);
+    }
+  }
+}
+
+
 }  // namespace lane
 }  // namespace kq
