@@ -336,10 +336,16 @@ def run_workload(args):
             yg = torch.empty((M, top_k, F), dtype=torch.float32, device=dev)
             yu = torch.empty_like(yg)
             yd = torch.empty((M, H), dtype=torch.float32, device=dev)
-            ysh = torch.empty((M, SH), dtype=torch.float32, device=dev)
+            ysg = torch.empty((M, SH), dtype=torch.float32, device=dev)
+            ysu = torch.empty_like(ysg)
             ysd = torch.empty((M, H), dtype=torch.float32, device=dev)
             wsg = kq.moe_workspace(F, M, top_k, E)
             wsd = kq.moe_workspace(H, M, top_k, E)
+            if M == 1:  # one token: the shared gate|up (same x) as one barrier-free chain launch
+                for L in per_layer:
+                    L["shared_gu"] = kq.Chain([
+                        {"type": synth.Q4_K, "x_dtype": kq.KQ_BF16, "W": L["Sg"], "x": x, "y": ysg, "N": SH, "K": H},
+                        {"type": synth.Q4_K, "x_dtype": kq.KQ_BF16, "W": L["Su"], "x": x, "y": ysu, "N": SH, "K": H}])
 
             def step():
                 for L in per_layer:
@@ -349,8 +355,11 @@ def run_workload(args):
                                      wsg, wsg.numel(), stream)
                     kq.kq_moe_matvec(synth.Q4_K, L["Wd"], E, L["ids"], L["gate"], xs, kq.KQ_BF16, 1, yd, H, F, M,
                                      top_k, wsd, wsd.numel(), stream)
-                    kq.kq_matvec(synth.Q4_K, L["Sg"], x, kq.KQ_BF16, ysh, SH, H, M, stream)
-                    kq.kq_matvec(synth.Q4_K, L["Su"], x, kq.KQ_BF16, ysh, SH, H, M, stream)
+                    if M == 1:
+                        L["shared_gu"].run(stream)
+                    else:
+                        kq.kq_matvec(synth.Q4_K, L["Sg"], x, kq.KQ_BF16, ysg, SH, H, M, stream)
+                        kq.kq_matvec(synth.Q4_K, L["Su"], x, kq.KQ_BF16, ysu, SH, H, M, stream)
                     kq.kq_matvec(synth.Q4_K, L["Sd"], xsh, kq.KQ_BF16, ysd, H, SH, M, stream)
             ms = _timed_graph(torch, step, stream, args.steps, args.warmup)
             kq.kq_moe_check(wsg)
@@ -360,7 +369,7 @@ def run_workload(args):
             nbytes = sum(L["nexp"] * eb + sb for L in per_layer)
             line(f"routed MoE decode, 30 layers, 128 experts top-8 + shared FFN, Q4_K, M={M}", nbytes, ms,
                  {"tok_s_equiv": M * 1e3 / ms, "distinct_experts_per_layer": sum(L["nexp"] for L in per_layer) / layers,
-                  "launches_per_step": 6 * layers})
+                  "launches_per_step": (5 if M == 1 else 6) * layers})
             del per_layer
             torch.cuda.empty_cache()
     else:

@@ -214,6 +214,16 @@ def test_matvec_m16_ragged(qtype, NK):
 
 
 @pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("NK", [(1, 256), (129, 704), (300, 2816), (128, 4096 + 96), (2600, 9728)])
+def test_matvec_two_tokens_ragged(qtype, NK):
+    """M = 2 with bf16 x runs the one-token kernel with two x images: ragged
+    tiles, K tails, and tile heights of 32, 16 and 8 rows."""
+    N, K = NK
+    y, yr, sr = _matvec_case(qtype, N, K, 2, "bf16", 211)
+    assert rel_err(y, yr, sr) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("qtype", TYPES)
 @pytest.mark.parametrize("xd", ["f32", "bf16"])
 def test_matvec_x_extreme_runs(qtype, xd):
     """Runs of x whose maximum is subnormal, tiny, huge or zero take the
@@ -232,3 +242,8 @@ def test_matvec_x_extreme_runs(qtype, xd):
     y = kq.matvec(qtype, dev(W), x_dev(x), N, K).cpu().numpy()
     yr, sr = oracle.matvec(qtype, W, N, K, x, threads=8)
     assert rel_err(y, yr, sr) <= TOL[xd]
+    if xd == "bf16":  # the two-token path stages each token's runs on its own
+        x2 = np.concatenate([synth.gen_x(1, K, g, "bf16"), x], axis=0)
+        y2 = kq.matvec(qtype, dev(W), x_dev(x2), N, K).cpu().numpy()
+        yr2, sr2 = oracle.matvec(qtype, W, N, K, x2, threads=8)
+        assert rel_err(y2, yr2, sr2) <= TOL[xd]
