@@ -105,7 +105,9 @@ kq_status kq_dequant(int type, const void *blocks, float *out, int64_t n, kq_str
  * the fly (each weight byte is read from memory once per call).
  *   x_dtype KQ_F32 or KQ_BF16; M in 1..16; K a multiple of 32.
  * Accumulation is fp32 in a fixed order, so repeated calls give identical y;
- * the order (hence the last bits of y) differs between M = 1 and M > 1.
+ * the order (hence the last bits of y) differs between paths: M = 1, and
+ * M = 2 with bf16 x (exact integer dots per block); M = 3..16 with bf16 x
+ * (tensor cores, weights rounded to bf16); M >= 2 with fp32 x.
  */
 kq_status kq_matvec(int type, const void *W, const void *x, int x_dtype, float *y, int64_t N, int64_t K,
                     int64_t M, kq_stream_t stream);
