@@ -214,6 +214,21 @@ def test_matvec_m16_ragged(qtype, NK):
 
 
 @pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("NK", [(300, 2816), (4096, 4096), (2560, 9728)])
+def test_matvec_two_tokens_bit_identical_to_one(qtype, NK):
+    """Two tokens (bf16 x) run the one-token arithmetic on two x images: each
+    row of the pair equals that token's one-token product bit for bit (the
+    property the ANE page tests for its few-token kernel)."""
+    N, K = NK
+    g = synth.rng(212, qtype, N, K)
+    W = dev(synth.gen_matrix(qtype, N, K, g))
+    x = x_dev(synth.gen_x(2, K, g, "bf16"))
+    y2 = kq.matvec(qtype, W, x, N, K)
+    for m in range(2):
+        assert torch.equal(y2[m], kq.matvec(qtype, W, x[m:m + 1], N, K)[0]), m
+
+
+@pytest.mark.parametrize("qtype", TYPES)
 @pytest.mark.parametrize("NK", [(1, 256), (129, 704), (300, 2816), (128, 4096 + 96), (2600, 9728)])
 def test_matvec_two_tokens_ragged(qtype, NK):
     """M = 2 with bf16 x runs the one-token kernel with two x images: ragged
