@@ -57,10 +57,17 @@ def build_model(torch, synth, seed=0):
     stages = synth.dense_layer_sweep()
     dev = torch.device("cuda")
     mats, xs = [], []
+    # every stage's x is a view of one device buffer (xs[0]._base), so a
+    # step's inputs arrive with one host-to-device copy
+    xbuf = torch.empty(sum(st[0][3] for st in stages), dtype=torch.bfloat16, device=dev)
+    off = 0
     for si, st in enumerate(stages):
         K = st[0][3]
         g = synth.rng(seed, 1000 + si)
-        xs.append(torch.from_numpy(synth.gen_x(1, K, g, "bf16").view(np.int16)).to(dev).view(torch.bfloat16))
+        xv = xbuf[off:off + K].view(1, K)
+        xv.copy_(torch.from_numpy(synth.gen_x(1, K, g, "bf16").view(np.int16)).to(dev).view(torch.bfloat16))
+        xs.append(xv)
+        off += K
         for (name, qt, N, K_) in st:
             gm = synth.rng(seed, 1000 + si, zlib.crc32(name.encode()) & 0xFFFF)
             kw = {"q6_scale_range": (-32, 31)} if qt == synth.Q6_K else {}
@@ -497,15 +504,15 @@ def main():
 
     # end to end: per step, H2D of the step's inputs from pinned host memory,
     # the step, and D2H of the logits (the step's result)
-    x_host = [x.cpu().pin_memory() for x in xs]
+    xbuf = xs[0]._base  # all stages' x, contiguous
+    x_host = xbuf.cpu().pin_memory()
     logits = mats[-1]["y"]
     logits_host = torch.empty_like(logits, device="cpu").pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in x_host)
+    h2d = x_host.numel() * x_host.element_size()
     d2h = logits.numel() * logits.element_size()
 
     def e2e_step():
-        for xd, xh in zip(xs, x_host):
-            xd.copy_(xh, non_blocking=True)
+        xbuf.copy_(x_host, non_blocking=True)
         step_graph.replay()
         logits_host.copy_(logits, non_blocking=True)
 
