@@ -124,7 +124,7 @@ __device__ __forceinline__ int first_unit(const KqOp& o, int cta, int G) {
 // stage of whole rows is one contiguous block: lane 0 copies its 16-byte
 // aligned superset with one bulk copy (fewer, larger copies stream faster).
 __device__ __forceinline__ void produce(const KqOp& o, int tile, int b0, int n, uint8_t* slot, uint64_t* full,
-                                       int lane, int BB) {
+                                       int lane, int BB, uint64_t pol) {
   const int64_t r0 = static_cast<int64_t>(tile) * (8 * o.R);
   if (o.contig) {
     if (lane == 0) {
@@ -132,7 +132,7 @@ __device__ __forceinline__ void produce(const KqOp& o, int tile, int b0, int n, 
       const uintptr_t s0 = reinterpret_cast<uintptr_t>(o.W + r0 * o.row_bytes);
       const uintptr_t as = s0 & ~uintptr_t(15), ae = (s0 + nrows * o.row_bytes + 15) & ~uintptr_t(15);
       mbar_arrive_expect_tx(full, static_cast<uint32_t>(ae - as));
-      bulk_g2s(slot, reinterpret_cast<const void*>(as), static_cast<uint32_t>(ae - as), full);
+      bulk_g2s_hint(slot, reinterpret_cast<const void*>(as), static_cast<uint32_t>(ae - as), full, pol);
     }
     return;
   }
@@ -149,7 +149,7 @@ __device__ __forceinline__ void produce(const KqOp& o, int tile, int b0, int n, 
   const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, len);
   if (lane == 0) mbar_arrive_expect_tx(full, total);
   __syncwarp();
-  if (len) bulk_g2s(slot + lane * o.srb, src, len, full);
+  if (len) bulk_g2s_hint(slot + lane * o.srb, src, len, full, pol);
 }
 
 // Grid barrier arrival: a release add (cumulative: it publishes every write
@@ -446,6 +446,7 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
     pdl_launch_dependents();
     int q = 0, slot = 0;
     uint32_t lap = 0;  // parity of the ring lap
+    const uint64_t pol = l2_evict_first_policy();  // weights are read once per launch
     StageCursor cc;
     cur_start<PROG>(a, cc, cta, G);
     while (cc.valid) {
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
       }
       produce(cc.o, cc.tile, cc.b0, min(cc.o.KC, cc.kb1 - cc.b0), rg.base + static_cast<size_t>(slot) * a.slot,
-              &rg.full[slot], lane, block_bytes_of(cc.o.type));
+              &rg.full[slot], lane, block_bytes_of(cc.o.type), pol);
       cur_next<PROG>(a, cc, cta, G);
       ++q;
       if (++slot == a.S) { slot = 0; lap ^= 1u; }
