@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
     mbar_init(bar, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ae - as));
-    bulk_g2s(tile_buf, reinterpret_cast<const void*>(as), static_cast<uint32_t>(ae - as), bar);
+    bulk_g2s_hint(tile_buf, reinterpret_cast<const void*>(as), static_cast<uint32_t>(ae - as), bar,
+                  l2_evict_first_policy());  // an expert tile is read once per call
   }
 
   // ---- the expert's pairs in (m, slot) order, and its plan offset

@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(NTH_TC, 1) tc_kernel(const __grid_constant__ T
   if (warp == NDQ) {
     // ------------------------------------------------------------- producer
     pdl_launch_dependents();
+    const uint64_t pol = l2_evict_first_policy();  // the weights are read once per launch
     bool failed = false;
     for (int k = 0; k < nst && !failed; ++k) {
       const int slot = k % a.Sraw;
@@ -259,10 +260,10 @@ __global__ void __launch_bounds__(NTH_TC, 1) tc_kernel(const __grid_constant__ T
         if (lane == 0) {
           mbar_arrive_expect_tx(&raw_full[slot], static_cast<uint32_t>(TR * a.srb));
           asm volatile(
-              "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-              "%3}], [%4];" ::"r"(smem_u32(sp)),
+              "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+              "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(sp)),
               "l"(reinterpret_cast<uint64_t>(&a.tmap)), "r"(b0 * BB / 4), "r"(static_cast<int>(row0)),
-              "r"(smem_u32(&raw_full[slot]))
+              "r"(smem_u32(&raw_full[slot])), "l"(pol)
               : "memory");
         }
         __syncwarp();
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(NTH_TC, 1) tc_kernel(const __grid_constant__ T
       __syncwarp();
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        if (len[i]) bulk_g2s(sp + (lane + 32 * i) * a.srb, src[i], len[i], &raw_full[slot]);
+        if (len[i]) bulk_g2s_hint(sp + (lane + 32 * i) * a.srb, src[i], len[i], &raw_full[slot], pol);
     }
     if (lane == 0)  // leave only after the copies in flight have landed (bounded)
       for (int k = (nst > a.Sraw ? nst - a.Sraw : 0); k < nst; ++k)
