@@ -1,5 +1,6 @@
-// kq_gemv.cu -- one-token products y = W x (M = 1) against Q4_K / Q5_K / Q6_K
-// rows: a single matrix, or a program of matrices run by one persistent launch.
+// kq_gemv.cu -- one-token products y = W x (M = 1; also M = 2 with bf16 x)
+// against Q4_K / Q5_K / Q6_K rows: a single matrix, or a program of matrices
+// run by one persistent launch.
 //
 // "GGUF in transformers", section "Reusing ggml's Metal kernels": decode-time
 // products read the packed super-blocks directly and dequantize on the fly;
@@ -30,8 +31,10 @@
 //  * the producer walks the CTA's units -- (tile of TT rows, K-part) of every
 //    op, in op order -- and keeps a CTA-wide ring of S shared-memory slots
 //    full with 1-D TMA bulk copies: one copy per stage when a stage holds
-//    whole rows, else one copy per row segment of KC blocks.  Weights never
-//    depend on earlier ops, so the producer runs ahead across op boundaries;
+//    whole rows, else one copy per row segment of KC blocks, all with an L2
+//    evict-first policy (weights are read once; activations stay in L2).
+//    Weights never depend on earlier ops, so the producer runs ahead across
+//    op boundaries;
 //  * a stage's blocks are dealt to the consumer warps round-robin (continuing
 //    across stages); quad q of a warp owns the tile rows q, q+8, ... (R of
 //    them: a tile is 8R rows), so one x slice, loaded once per block, serves
