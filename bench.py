@@ -52,6 +52,21 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def max_over_ranks(torch, dist, value, device):
+    """The largest of every rank's value, on every rank (the slowest replica
+    sets the whole job's time); dist None: one process."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_replica, world, ms):
+    """Whole-job throughput: every replica reads its own weights once per step."""
+    return bytes_per_replica * world / (ms * 1e-3) / 1e9
+
+
 def build_model(torch, synth, seed=0):
     """Weights and per-stage inputs/outputs for one token of the sweep."""
     stages = synth.dense_layer_sweep()
@@ -465,12 +480,7 @@ def main():
     variants = {}
     with ClockSampler(local) as clk:
         for name, graph in graphs.items():
-            t = timed(graph, args.steps)
-            if dist is not None:
-                tt = torch.tensor([t], device="cuda")
-                dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-                t = float(tt.item())
-            variants[name] = t
+            variants[name] = max_over_ranks(torch, dist, timed(graph, args.steps), "cuda")
     assert kq.kq_device_error() == 0, "device error word set"
     best = min(variants, key=variants.get)
     ms = variants[best]
@@ -526,18 +536,14 @@ def main():
             e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / args.steps, "cuda")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(host_sample(synth, n_mats=7))
 
     if rank == 0:
-        gbs = total_bytes * world / (ms * 1e-3) / 1e9
+        gbs = job_gbs(total_bytes, world, ms)
         line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
                 "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "u8 codes x bf16 x, int32/fp32 accumulate", "data": "synthetic",
