@@ -335,6 +335,27 @@ def run_workload(args):
             tot_ms += ms
         line("verify block M=16, gate/up 4096->14336, down 14336->4096, Q4_K, bf16 x", tot_b, tot_ms,
              {"cases": res, "tok_s_equiv": 16e3 / tot_ms})
+    elif wl == "dequant":
+        # expansion to fp32 / bf16 (the dequantizing load path): bytes read + written per second
+        res = {}
+        for qt, nm in ((synth.Q4_K, "Q4_K"), (synth.Q5_K, "Q5_K"), (synth.Q6_K, "Q6_K")):
+            N, K = 14336, 4096
+            W0 = synth.gen_matrix(qt, N, K, synth.rng(6, qt))
+            ncopy = max(2, -(-L2_SPAN // W0.size))
+            Ws = [torch.from_numpy(W0).to(dev) for _ in range(ncopy)]
+            out32 = torch.empty(N * K, dtype=torch.float32, device=dev)
+            out16 = torch.empty(N * K, dtype=torch.bfloat16, device=dev)
+            for tag, out, fn, ob in (("fp32", out32, kq.kq_dequant, 4), ("bf16", out16, kq.kq_dequant_bf16, 2)):
+                def step(out=out, fn=fn):
+                    for W in Ws:
+                        fn(qt, W, out, N * K, stream)
+                ms = _timed_graph(torch, step, stream, args.steps, args.warmup) / ncopy
+                moved = W0.size + N * K * ob
+                res[f"{nm}/{tag}"] = {"ms": ms, "GB/s": moved / (ms * 1e-3) / 1e9, "read": W0.size, "written": N * K * ob}
+        tot_b = sum(v["read"] + v["written"] for v in res.values())
+        tot_ms = sum(v["ms"] for v in res.values())
+        line("dequant 14336x4096 to fp32 and bf16, Q4_K/Q5_K/Q6_K (GB/s of bytes read + written)", tot_b, tot_ms,
+             {"cases": res})
     elif wl == "moe":
         E, H, F, SH, top_k, layers = 128, 2816, 704, 2112, 8, 30
         for M in (1, 16):
@@ -407,7 +428,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single", default=None,
                     help="profiling helper: run one product TYPE:NxK[:M[:f32|bf16]] (e.g. Q4_K:19456x2560) --steps times")
-    ap.add_argument("--workload", default=None, choices=["q4k_4096", "format_sweep", "verify16", "moe"],
+    ap.add_argument("--workload", default=None, choices=["q4k_4096", "format_sweep", "verify16", "moe", "dequant"],
                     help="time another configuration instead of the dense sweep (one JSON line each)")
     args = ap.parse_args()
     if args.workload:

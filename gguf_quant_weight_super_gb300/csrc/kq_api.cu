@@ -80,7 +80,17 @@ kq_status kq_dequant(int type, const void* blocks, float* out, int64_t n, kq_str
   if (n == 0) return KQ_OK;
   if (!blocks || !out) return KQ_ERR_ARG;
   if (!aligned(blocks, 16) || !aligned(out, 16)) return KQ_ERR_ALIGN;
-  return cuda_status(launch_dequant(type, blocks, out, n / 256, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_dequant(type, blocks, out, 0, n / 256, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kq_status kq_dequant_bf16(int type, const void* blocks, uint16_t* out, int64_t n, kq_stream_t stream) {
+  if (!valid_type(type)) return KQ_ERR_TYPE;
+  if (n < 0) return KQ_ERR_ARG;
+  if (n % 256) return KQ_ERR_SHAPE;
+  if (n == 0) return KQ_OK;
+  if (!blocks || !out) return KQ_ERR_ARG;
+  if (!aligned(blocks, 16) || !aligned(out, 16)) return KQ_ERR_ALIGN;
+  return cuda_status(launch_dequant(type, blocks, out, 1, n / 256, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kq_status kq_matvec(int type, const void* W, const void* x, int x_dtype, float* y, int64_t N, int64_t K, int64_t M,

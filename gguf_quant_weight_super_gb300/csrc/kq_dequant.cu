@@ -19,8 +19,16 @@ namespace {
 constexpr int THREADS = 256;
 constexpr int GROUPS = THREADS / 8;  // one 8-lane group per block
 
-template <int QT>
-__global__ void __launch_bounds__(THREADS) dequant_kernel(const uint8_t* __restrict__ blocks, float* __restrict__ out,
+// Two fp32 weights as one bf16 pair, each rounded to nearest even (lo in the low half).
+__device__ __forceinline__ uint32_t bf16_pair(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// OutT float: fp32 weights; OutT uint16_t: the same weights rounded to bf16.
+template <int QT, typename OutT>
+__global__ void __launch_bounds__(THREADS) dequant_kernel(const uint8_t* __restrict__ blocks, OutT* __restrict__ out,
                                                           int64_t n_blocks) {
   constexpr int BB = Fmt<QT>::BYTES;
   constexpr int P = Fmt<QT>::P;
@@ -32,7 +40,7 @@ __global__ void __launch_bounds__(THREADS) dequant_kernel(const uint8_t* __restr
     lane_fields<QT>(blocks + b * BB, j, fl);
     const float d = half_bits_to_float(fl.d_bits);
     const float dmin = half_bits_to_float(fl.dmin_bits);
-    float* o = out + b * 256;
+    OutT* o = out + b * 256;
 #pragma unroll
     for (int p = 0; p < P; ++p) {
       const float dsc = d * static_cast<float>(fl.sc[p]);
@@ -44,9 +52,17 @@ __global__ void __launch_bounds__(THREADS) dequant_kernel(const uint8_t* __restr
         if constexpr (QT == T_Q6_K) w[i] = dsc * (q - 32.0f);
         else w[i] = __fmaf_rn(dsc, q, -mm);
       }
-      float* dst = o + part_pos<QT>(j, p);
+      OutT* dst = o + part_pos<QT>(j, p);
+      if constexpr (sizeof(OutT) == 4) {
 #pragma unroll
-      for (int i = 0; i < L; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(w[i], w[i + 1], w[i + 2], w[i + 3]);
+        for (int i = 0; i < L; i += 4)
+          *reinterpret_cast<float4*>(dst + i) = make_float4(w[i], w[i + 1], w[i + 2], w[i + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < L; i += 8)
+          *reinterpret_cast<uint4*>(dst + i) = make_uint4(bf16_pair(w[i], w[i + 1]), bf16_pair(w[i + 2], w[i + 3]),
+                                                          bf16_pair(w[i + 4], w[i + 5]), bf16_pair(w[i + 6], w[i + 7]));
+      }
     }
   }
 }
@@ -88,14 +104,20 @@ int grid_for(int64_t n_blocks) {
 
 }  // namespace
 
-cudaError_t launch_dequant(int qtype, const void* blocks, float* out, int64_t n_blocks, cudaStream_t stream) {
+cudaError_t launch_dequant(int qtype, const void* blocks, void* out, int out_bf16, int64_t n_blocks,
+                           cudaStream_t stream) {
   if (n_blocks == 0) return cudaSuccess;
   const uint8_t* b = static_cast<const uint8_t*>(blocks);
   const int grid = grid_for(n_blocks);
-  switch (qtype) {
-    case T_Q4_K: dequant_kernel<T_Q4_K><<<grid, THREADS, 0, stream>>>(b, out, n_blocks); break;
-    case T_Q5_K: dequant_kernel<T_Q5_K><<<grid, THREADS, 0, stream>>>(b, out, n_blocks); break;
-    case T_Q6_K: dequant_kernel<T_Q6_K><<<grid, THREADS, 0, stream>>>(b, out, n_blocks); break;
+  float* of = static_cast<float*>(out);
+  uint16_t* oh = static_cast<uint16_t*>(out);
+  switch (qtype * 2 + (out_bf16 ? 1 : 0)) {
+    case T_Q4_K * 2: dequant_kernel<T_Q4_K, float><<<grid, THREADS, 0, stream>>>(b, of, n_blocks); break;
+    case T_Q5_K * 2: dequant_kernel<T_Q5_K, float><<<grid, THREADS, 0, stream>>>(b, of, n_blocks); break;
+    case T_Q6_K * 2: dequant_kernel<T_Q6_K, float><<<grid, THREADS, 0, stream>>>(b, of, n_blocks); break;
+    case T_Q4_K * 2 + 1: dequant_kernel<T_Q4_K, uint16_t><<<grid, THREADS, 0, stream>>>(b, oh, n_blocks); break;
+    case T_Q5_K * 2 + 1: dequant_kernel<T_Q5_K, uint16_t><<<grid, THREADS, 0, stream>>>(b, oh, n_blocks); break;
+    case T_Q6_K * 2 + 1: dequant_kernel<T_Q6_K, uint16_t><<<grid, THREADS, 0, stream>>>(b, oh, n_blocks); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -82,7 +82,8 @@ cudaError_t launch_moe_static(int qtype, const void* W, int n_experts, const int
                               const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M,
                               int top_k, cudaStream_t st);
 
-cudaError_t launch_dequant(int qtype, const void* blocks, float* out, int64_t n_blocks, cudaStream_t stream);
+cudaError_t launch_dequant(int qtype, const void* blocks, void* out, int out_bf16, int64_t n_blocks,
+                           cudaStream_t stream);
 cudaError_t launch_unpack(int qtype, const void* blocks, int64_t n_blocks, uint8_t* codes, int8_t* scales,
                           uint8_t* mins, uint16_t* d_bits, uint16_t* dmin_bits, cudaStream_t stream);
 

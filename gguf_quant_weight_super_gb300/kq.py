@@ -27,6 +27,7 @@ SIGNATURES = {
     "kq_block_bytes": (_SZ, [_I]),
     "kq_unpack": (_I, [_I, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "kq_dequant": (_I, [_I, _P, _P, _I64, _P]),
+    "kq_dequant_bf16": (_I, [_I, _P, _P, _I64, _P]),
     "kq_matvec": (_I, [_I, _P, _P, _I, _P, _I64, _I64, _I64, _P]),
     "kq_chain_workspace_size": (_SZ, [_P, _I]),
     "kq_chain_prepare": (_I, [_P, _I, _P, _SZ, _P, _P]),
@@ -130,6 +131,10 @@ def kq_unpack(qtype, blocks, n_blocks, codes=None, scales=None, mins=None, d_bit
 
 def kq_dequant(qtype, blocks, out, n, stream=None):
     _check("kq_dequant", lib().kq_dequant(qtype, _ptr(blocks), _ptr(out), n, _stream(stream)))
+
+
+def kq_dequant_bf16(qtype, blocks, out, n, stream=None):
+    _check("kq_dequant_bf16", lib().kq_dequant_bf16(qtype, _ptr(blocks), _ptr(out), n, _stream(stream)))
 
 
 def kq_matvec(qtype, W, x, x_dtype, y, N, K, M, stream=None):
@@ -260,4 +265,11 @@ class Chain:
 def dequant(qtype: int, blocks: torch.Tensor, n: int) -> torch.Tensor:
     out = torch.empty(n, dtype=torch.float32, device=blocks.device)
     kq_dequant(qtype, blocks, out, n)
+    return out
+
+
+def dequant_bf16(qtype: int, blocks: torch.Tensor, n: int) -> torch.Tensor:
+    """The weights as a torch.bfloat16 tensor (kq_dequant_bf16)."""
+    out = torch.empty(n, dtype=torch.bfloat16, device=blocks.device)
+    kq_dequant_bf16(qtype, blocks, out, n)
     return out

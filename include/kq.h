@@ -101,6 +101,17 @@ kq_status kq_unpack(int type, const void *blocks, int64_t n_blocks, uint8_t *cod
 kq_status kq_dequant(int type, const void *blocks, float *out, int64_t n, kq_stream_t stream);
 
 /*
+ * The same weights as kq_dequant, written as bfloat16 bit patterns: out[i] is
+ * kq_dequant's fp32 out[i] rounded to the nearest bf16, ties to even (a NaN
+ * stays a NaN).  The expansion "GGUF in transformers" describes for
+ * GgufConfig(dequantize=True, dtype=torch.bfloat16) ("Load GGUF with
+ * transformers"), at half the bytes written of the fp32 form.
+ * blocks: 16-byte aligned.  out: 16-byte aligned, n uint16 values.  n a
+ * multiple of 256.  Errors as kq_dequant.
+ */
+kq_status kq_dequant_bf16(int type, const void *blocks, uint16_t *out, int64_t n, kq_stream_t stream);
+
+/*
  * y[m][n] = sum_{k<K} w[n][k] * x[m][k] for m < M, n < N, dequantizing W on
  * the fly (each weight byte is read from memory once per call).
  *   x_dtype KQ_F32 or KQ_BF16; M in 1..16; K a multiple of 32.

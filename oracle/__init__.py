@@ -134,6 +134,25 @@ def dequant(qtype: int, blocks: np.ndarray) -> np.ndarray:
     return out
 
 
+def f32_to_bf16_bits(f: np.ndarray) -> np.ndarray:
+    """fp32 -> bfloat16 bit patterns, rounded to nearest, ties to even (the
+    plain definition: keep the top 16 bits after adding half an ulp of the
+    kept part, plus one if that part is odd); a NaN stays a NaN (quiet, sign
+    kept)."""
+    u = np.ascontiguousarray(f, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    nan = ((u & 0x7F800000) == 0x7F800000) & ((u & 0x7FFFFF) != 0)
+    r[nan] = ((u[nan] >> 16) | 0x0040).astype(np.uint16)
+    return r
+
+
+def dequant_bf16(qtype: int, blocks: np.ndarray) -> np.ndarray:
+    """All blocks -> the fp32 weights of dequant, rounded to bfloat16 (bit patterns).
+    "GGUF in transformers", "Load GGUF with transformers": GgufConfig(dequantize=True,
+    dtype=torch.bfloat16) expands the weights to bf16."""
+    return f32_to_bf16_bits(dequant(qtype, blocks))
+
+
 def _x_arg(x: np.ndarray):
     x = np.ascontiguousarray(x)
     if x.dtype == np.float32:

@@ -61,6 +61,11 @@ def test_argument_errors_without_gpu(L):
     assert L.kq_dequant(1, fake, fake, 100, None) == -3                        # n % 256
     assert L.kq_dequant(3, fake, P(0x1004), 256, None) == -5                   # out alignment
     assert L.kq_dequant(3, fake, fake, 0, None) == 0
+    assert L.kq_dequant_bf16(7, fake, fake, 256, None) == -2                   # type
+    assert L.kq_dequant_bf16(1, fake, fake, 300, None) == -3                   # n % 256
+    assert L.kq_dequant_bf16(2, fake, P(0x1008), 256, None) == -5              # out alignment
+    assert L.kq_dequant_bf16(2, None, fake, 256, None) == -1                   # null blocks
+    assert L.kq_dequant_bf16(3, fake, fake, 0, None) == 0
     assert L.kq_unpack(4, fake, 1, None, None, None, None, None, None) == -2
     assert L.kq_unpack(1, fake, -1, None, None, None, None, None, None) == -1
 

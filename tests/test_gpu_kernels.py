@@ -60,6 +60,25 @@ def test_unpack_bit_exact(qtype):
 
 @pytest.mark.parametrize("qtype", TYPES)
 @pytest.mark.parametrize("dist", ["workload", "random_bytes"])
+def test_dequant_bf16_bit_exact(qtype, dist):
+    """bf16 weights: the fp32 weights rounded to nearest even, bit for bit
+    (NaN blocks from random bytes stay NaN)."""
+    g = synth.rng(205, qtype)
+    nb = 4099
+    if dist == "workload":
+        blocks = synth.gen_blocks(qtype, nb, g)
+    else:
+        blocks = g.integers(0, 256, size=(nb, synth.BLOCK_BYTES[qtype]), dtype=np.uint8)
+    ref = oracle.dequant_bf16(qtype, blocks)
+    got = kq.dequant_bf16(qtype, dev(blocks.reshape(-1)), nb * 256).cpu().view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16).float().numpy())
+    gnan = np.isnan(torch.from_numpy(got.view(np.int16)).view(torch.bfloat16).float().numpy())
+    assert np.array_equal(gnan, nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("dist", ["workload", "random_bytes"])
 def test_dequant_bit_exact(qtype, dist):
     g = synth.rng(201, qtype)
     nb = 4099

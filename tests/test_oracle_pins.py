@@ -7,7 +7,9 @@
 * closed forms: constant fields, one-hot scales and mins, the Q6_K zero point;
 * the product against plain integer / float matrix products (numpy matmul) on
   tiny matrices, linearity in x, zero x, weights past K ignored;
-* the routed-expert product against per-slot products and brute force.
+* the routed-expert product against per-slot products and brute force;
+* the bf16 rounding of dequantized weights against torch's bfloat16 conversion
+  and hand-worked ties.
 
 All run on the CPU.
 """
@@ -311,3 +313,38 @@ def test_moe_group_by_definition():
     assert experts == [0, 1, 4]
     assert offsets == [0, 1, 3, 5]
     assert pairs == [3, 1, 2, 0, 5]
+
+
+def test_bf16_rounding_against_torch_and_ties():
+    """f32 -> bf16 rounding (used by the bf16 dequant oracle): every one of a
+    few hundred thousand patterns -- random bits, exact ties, subnormals,
+    infinities, the largest floats -- agrees with torch's conversion, and the
+    hand-worked ties go to the even neighbour."""
+    import oracle
+    g = np.random.default_rng(114)
+    u = g.integers(0, 2**32, size=200000, dtype=np.uint64).astype(np.uint32)
+    ties = (g.integers(0, 2**16, size=50000, dtype=np.uint64).astype(np.uint32) << 16) | 0x8000
+    special = np.array([0, 0x80000000, 0x00000001, 0x007FFFFF, 0x00008000, 0x00018000, 0x7F7FFFFF,
+                        0x7F7F8000, 0xFF7FFFFF, 0x7F800000, 0xFF800000, 0x3F808000, 0x3F818000,
+                        0x3F808001, 0x3F807FFF], dtype=np.uint32)
+    allu = np.concatenate([u, ties, special])
+    f = allu.view(np.float32)
+    got = oracle.f32_to_bf16_bits(f)
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(f)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.all(np.isnan(torch.from_numpy(got[nan].view(np.int16)).view(torch.bfloat16).float().numpy()))
+    # ties to even: 1 + 2^-8 -> 1.0 (0x3F80), 1 + 3*2^-8 -> 1 + 2^-6 (0x3F82); just past a tie rounds up
+    t = np.array([0x3F808000, 0x3F818000, 0x3F808001, 0x3F807FFF], dtype=np.uint32).view(np.float32)
+    assert oracle.f32_to_bf16_bits(t).tolist() == [0x3F80, 0x3F82, 0x3F81, 0x3F80]
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+def test_dequant_bf16_is_the_fp32_weights_rounded(orc, qtype):
+    """The bf16 dequant oracle equals the fp32 oracle's weights converted by
+    torch (round to nearest even)."""
+    g = synth.rng(115, qtype)
+    blocks = synth.gen_blocks(qtype, 64, g)
+    w = orc.dequant(qtype, blocks)
+    ref = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(orc.dequant_bf16(qtype, blocks), ref)
