@@ -365,10 +365,11 @@ def run_workload(args):
             per_layer = []
             for li in range(layers):
                 gl = synth.rng(2, M, li)
-                ids, gate = synth.gen_routing(M, E, top_k, gl)
                 lay = {"Wg": torch.from_numpy(Wg0).to(dev), "Wu": torch.from_numpy(Wg0).to(dev),
-                       "Wd": torch.from_numpy(Wd0).to(dev), "ids": torch.from_numpy(ids).to(dev),
-                       "gate": torch.from_numpy(gate).to(dev), "nexp": len(set(ids.reshape(-1).tolist())),
+                       "Wd": torch.from_numpy(Wd0).to(dev),
+                       "logits": torch.from_numpy(synth.gen_logits(M, E, gl)).to(dev),
+                       "ids": torch.empty((M, top_k), dtype=torch.int32, device=dev),
+                       "gate": torch.empty((M, top_k), dtype=torch.float32, device=dev),
                        "Sg": torch.from_numpy(synth.gen_matrix(synth.Q4_K, SH, H, gl)).to(dev),
                        "Su": torch.from_numpy(synth.gen_matrix(synth.Q4_K, SH, H, gl)).to(dev),
                        "Sd": torch.from_numpy(synth.gen_matrix(synth.Q4_K, H, SH, gl)).to(dev)}
@@ -390,8 +391,13 @@ def run_workload(args):
                         {"type": synth.Q4_K, "x_dtype": kq.KQ_BF16, "W": L["Sg"], "x": x, "y": ysg, "N": SH, "K": H},
                         {"type": synth.Q4_K, "x_dtype": kq.KQ_BF16, "W": L["Su"], "x": x, "y": ysu, "N": SH, "K": H}])
 
+            def route_all():
+                for L in per_layer:
+                    kq.kq_moe_route(L["logits"], M, E, top_k, L["ids"], L["gate"], None, stream)
+
             def step():
                 for L in per_layer:
+                    kq.kq_moe_route(L["logits"], M, E, top_k, L["ids"], L["gate"], None, stream)
                     kq.kq_moe_matvec(synth.Q4_K, L["Wg"], E, L["ids"], None, x, kq.KQ_BF16, 0, yg, F, H, M, top_k,
                                      wsg, wsg.numel(), stream)
                     kq.kq_moe_matvec(synth.Q4_K, L["Wu"], E, L["ids"], None, x, kq.KQ_BF16, 0, yu, F, H, M, top_k,
@@ -407,12 +413,16 @@ def run_workload(args):
             ms = _timed_graph(torch, step, stream, args.steps, args.warmup)
             kq.kq_moe_check(wsg)
             kq.kq_moe_check(wsd)
+            route_ms = _timed_graph(torch, route_all, stream, args.steps, args.warmup)
+            for L in per_layer:  # distinct experts the router picked (the expert bytes a step reads)
+                L["nexp"] = int(torch.unique(L["ids"]).numel())
             eb = synth.matrix_bytes(synth.Q4_K, F, H) * 2 + synth.matrix_bytes(synth.Q4_K, H, F)
             sb = synth.matrix_bytes(synth.Q4_K, SH, H) * 2 + synth.matrix_bytes(synth.Q4_K, H, SH)
             nbytes = sum(L["nexp"] * eb + sb for L in per_layer)
-            line(f"routed MoE decode, 30 layers, 128 experts top-8 + shared FFN, Q4_K, M={M}", nbytes, ms,
+            line(f"routed MoE decode, 30 layers, router + 128 experts top-8 + shared FFN, Q4_K, M={M}", nbytes, ms,
                  {"tok_s_equiv": M * 1e3 / ms, "distinct_experts_per_layer": sum(L["nexp"] for L in per_layer) / layers,
-                  "launches_per_step": (5 if M == 1 else 6) * layers})
+                  "launches_per_step": (6 if M == 1 else 7) * layers,
+                  "router_us_per_layer": route_ms * 1e3 / layers})
             del per_layer
             torch.cuda.empty_cache()
     else:

@@ -258,6 +258,21 @@ kq_status kq_moe_matvec_noalloc(int type, const void* W_experts, int32_t n_exper
   return cuda_status(e);
 }
 
+kq_status kq_moe_route(const float* logits, int64_t M, int32_t n_experts, int32_t top_k, int32_t* expert_ids,
+                       float* gate_w, void* workspace, size_t workspace_bytes, kq_stream_t stream) {
+  if (M < 0 || n_experts <= 0 || top_k <= 0) return KQ_ERR_ARG;
+  if (M == 0) return KQ_OK;
+  if (!route_supported(M, n_experts, top_k)) return KQ_ERR_UNSUPPORTED;
+  if (!logits || !expert_ids || !gate_w) return KQ_ERR_ARG;
+  if (!aligned(logits, 4) || !aligned(expert_ids, 4) || !aligned(gate_w, 4)) return KQ_ERR_ALIGN;
+  if (workspace && (!aligned(workspace, 256) || workspace_bytes < route_plan_bytes(M, top_k, n_experts)))
+    return KQ_ERR_WORKSPACE;
+  cudaError_t e = launch_route(logits, static_cast<int>(M), n_experts, top_k, expert_ids, gate_w, workspace,
+                               reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_status(e);
+}
+
 kq_status kq_moe_check(void* workspace, kq_stream_t stream) {
   if (!workspace) return KQ_ERR_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

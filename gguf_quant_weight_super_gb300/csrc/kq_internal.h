@@ -82,6 +82,13 @@ cudaError_t launch_moe_static(int qtype, const void* W, int n_experts, const int
                               const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M,
                               int top_k, cudaStream_t st);
 
+// MoE router (kq_route.cu): top-k + softmax over the selected logits, and the
+// grouping plan (written at ws + 256 in kq_moe_matvec's layout when ws is set)
+bool route_supported(int64_t M, int E, int top_k);
+size_t route_plan_bytes(int64_t M, int top_k, int E);
+cudaError_t launch_route(const float* logits, int M, int E, int top_k, int* ids, float* gate, void* ws,
+                         cudaStream_t st);
+
 cudaError_t launch_dequant(int qtype, const void* blocks, void* out, int out_bf16, int64_t n_blocks,
                            cudaStream_t stream);
 cudaError_t launch_unpack(int qtype, const void* blocks, int64_t n_blocks, uint8_t* codes, int8_t* scales,

@@ -28,6 +28,7 @@ SIGNATURES = {
     "kq_unpack": (_I, [_I, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "kq_dequant": (_I, [_I, _P, _P, _I64, _P]),
     "kq_dequant_bf16": (_I, [_I, _P, _P, _I64, _P]),
+    "kq_moe_route": (_I, [_P, _I64, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _SZ, _P]),
     "kq_matvec": (_I, [_I, _P, _P, _I, _P, _I64, _I64, _I64, _P]),
     "kq_chain_workspace_size": (_SZ, [_P, _I]),
     "kq_chain_prepare": (_I, [_P, _I, _P, _SZ, _P, _P]),
@@ -131,6 +132,21 @@ def kq_unpack(qtype, blocks, n_blocks, codes=None, scales=None, mins=None, d_bit
 
 def kq_dequant(qtype, blocks, out, n, stream=None):
     _check("kq_dequant", lib().kq_dequant(qtype, _ptr(blocks), _ptr(out), n, _stream(stream)))
+
+
+def kq_moe_route(logits, M, n_experts, top_k, expert_ids, gate_w, workspace=None, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("kq_moe_route", lib().kq_moe_route(_ptr(logits), M, n_experts, top_k, _ptr(expert_ids), _ptr(gate_w),
+                                              _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def moe_route(logits: torch.Tensor, top_k: int, workspace=None, stream=None):
+    """(ids int32 [M, top_k], gate fp32 [M, top_k]) for logits [M, n_experts] (kq_moe_route)."""
+    M, E = logits.shape
+    ids = torch.empty((M, top_k), dtype=torch.int32, device=logits.device)
+    gate = torch.empty((M, top_k), dtype=torch.float32, device=logits.device)
+    kq_moe_route(logits, M, E, top_k, ids, gate, workspace, stream)
+    return ids, gate
 
 
 def kq_dequant_bf16(qtype, blocks, out, n, stream=None):

@@ -94,13 +94,20 @@ def gen_x(M: int, K: int, g: np.random.Generator, dtype: str = "f32") -> np.ndar
 
 
 def gen_routing(M: int, n_experts: int, top_k: int, g: np.random.Generator):
-    """(ids int32 [M, top_k], gate float32 [M, top_k]) from N(0,1) router logits."""
-    logits = g.standard_normal((M, n_experts))
-    ids = np.argsort(-logits, axis=1, kind="stable")[:, :top_k].astype(np.int32)
-    sel = np.take_along_axis(logits, ids.astype(np.int64), axis=1)
-    e = np.exp(sel - sel.max(axis=1, keepdims=True))
-    gate = (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+    """(ids int32 [M, top_k], gate float32 [M, top_k]): top_k distinct experts
+    per token drawn uniformly, positive gates summing to about 1 (a flat
+    Dirichlet draw).  Drawn directly, not by routing logits."""
+    ids = np.stack([g.permutation(n_experts)[:top_k] for _ in range(M)]).astype(np.int32).reshape(M, top_k)
+    gate = g.dirichlet(np.ones(top_k), size=M).astype(np.float32).reshape(M, top_k)
     return ids, gate
+
+
+def gen_logits(M: int, n_experts: int, g: np.random.Generator, ties: bool = False) -> np.ndarray:
+    """Router logits [M, n_experts] fp32: N(0, 1), or small integers (-4..4)
+    so that equal logits are common."""
+    if ties:
+        return g.integers(-4, 5, size=(M, n_experts)).astype(np.float32)
+    return g.standard_normal((M, n_experts), dtype=np.float32)
 
 
 # --------------------------------------------------------------------------

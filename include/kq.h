@@ -252,6 +252,33 @@ kq_status kq_moe_matvec_noalloc(int type, const void *W_experts, int32_t n_exper
 kq_status kq_moe_check(void *workspace, kq_stream_t stream);
 
 /*
+ * The MoE router: for each of M tokens, the top_k experts of its n_experts
+ * router logits and their gate weights, and optionally the grouping of the
+ * (token, slot) pairs by expert.
+ *
+ * "GGUF in transformers", "Reusing ggml's Metal kernels": a top-k kernel
+ * combining softmax and top-k routing; "ANE Fieldfare" README, "How it works"
+ * (8 of 128 experts per token) and "Speculative decoding" (a GPU planning
+ * kernel groups a verify block's tokens by expert).
+ *
+ *   logits      [M][n_experts] fp32 (device).
+ *   expert_ids  [M][top_k] int32: the top_k largest logits of each token in
+ *               descending order; equal logits in ascending expert order; a
+ *               NaN logit ranks below every number.
+ *   gate_w      [M][top_k] fp32: exp(l_j - l_0) / sum_i exp(l_i - l_0) over the
+ *               selected logits l_0 >= l_1 >= ... (a softmax over all experts,
+ *               renormalized over the selected ones).
+ *   workspace   NULL, or a kq_moe_matvec workspace (256-byte aligned): the
+ *               grouping is written in the plan layout kq_moe_matvec leaves
+ *               there (at byte 256: D, expert[Dmax], offset[Dmax+1], pairs),
+ *               Dmax = min(M*top_k, n_experts).
+ * Limits: M*top_k <= 512, n_experts <= 4096, 1 <= top_k <= min(32, n_experts)
+ * (else KQ_ERR_UNSUPPORTED).  Stream-ordered (programmatic dependent launch).
+ */
+kq_status kq_moe_route(const float *logits, int64_t M, int32_t n_experts, int32_t top_k, int32_t *expert_ids,
+                       float *gate_w, void *workspace, size_t workspace_bytes, kq_stream_t stream);
+
+/*
  * Read the device error word (KQ_OK when clean); with clear != 0 also reset
  * it.  Synchronizes the device.
  */

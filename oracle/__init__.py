@@ -195,6 +195,33 @@ def moe_matvec(qtype: int, W_experts: np.ndarray, n_experts: int, ids: np.ndarra
     return y, s
 
 
+def moe_route(logits: np.ndarray, top_k: int):
+    """The MoE router by definition (plain numpy, fp64 arithmetic).
+
+    "GGUF in transformers", "Reusing ggml's Metal kernels": a kernel combining
+    softmax and top-k routing; "ANE Fieldfare" README, "How it works": each
+    token picks 8 of 128 experts.  Reading: the top_k largest logits of a row in
+    descending order, equal logits in ascending index order, a NaN below every
+    number; gate_j = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the selected.
+    Returns (ids int32 [M, top_k], gate float64 [M, top_k])."""
+    logits = np.asarray(logits, dtype=np.float32)
+    M, E = logits.shape
+    ids = np.zeros((M, top_k), dtype=np.int32)
+    gate = np.zeros((M, top_k), dtype=np.float64)
+    for m in range(M):
+        row = logits[m].astype(np.float64)
+        nan = np.isnan(row)
+        neg = np.where(nan, 0.0, -row)  # ascending -value = descending value
+        order = np.lexsort((np.arange(E), neg, nan))  # NaN last, then value desc, then index asc
+        sel = order[:top_k]
+        ids[m] = sel
+        l = row[sel]
+        with np.errstate(invalid="ignore"):  # an infinite or NaN leading logit gives NaN gates
+            ex = np.exp(l - l[0])
+            gate[m] = ex / np.sum(ex)
+    return ids, gate
+
+
 def moe_group(ids: np.ndarray, n_experts: int):
     """Grouping of routed (token, slot) pairs by expert, by its definition:
     the distinct valid ids in ascending order, and for each the pair indices

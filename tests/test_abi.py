@@ -90,6 +90,24 @@ def test_chain_argument_errors_without_gpu(L):
         kq.kq_chain_prepare([ops()], 0x800010, 1 << 20, plan, stream=0)
 
 
+def test_route_argument_errors_without_gpu(L):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    r = L.kq_moe_route
+    assert r(fake, -1, 128, 8, fake, fake, None, 0, None) == -1        # M < 0
+    assert r(fake, 0, 128, 8, fake, fake, None, 0, None) == 0          # empty: no-op
+    assert r(fake, 4, 0, 8, fake, fake, None, 0, None) == -1           # no experts
+    assert r(fake, 4, 128, 0, fake, fake, None, 0, None) == -1         # top_k < 1
+    assert r(fake, 4, 6, 8, fake, fake, None, 0, None) == -4           # top_k > n_experts
+    assert r(fake, 4, 128, 33, fake, fake, None, 0, None) == -4        # top_k > 32
+    assert r(fake, 65, 128, 8, fake, fake, None, 0, None) == -4        # M*top_k > 512
+    assert r(fake, 4, 8192, 8, fake, fake, None, 0, None) == -4        # n_experts > 4096
+    assert r(None, 4, 128, 8, fake, fake, None, 0, None) == -1         # null logits
+    assert r(P(0x1002), 4, 128, 8, fake, fake, None, 0, None) == -5    # logits alignment
+    assert r(fake, 4, 128, 8, fake, fake, P(0x1080), 1 << 20, None) == -7  # workspace alignment
+    assert r(fake, 4, 128, 8, fake, fake, fake, 64, None) == -7        # workspace too small
+
+
 def test_moe_argument_errors_without_gpu(L):
     f = 0x100000
     def call(**kw):

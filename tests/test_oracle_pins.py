@@ -9,7 +9,8 @@
   tiny matrices, linearity in x, zero x, weights past K ignored;
 * the routed-expert product against per-slot products and brute force;
 * the bf16 rounding of dequantized weights against torch's bfloat16 conversion
-  and hand-worked ties.
+  and hand-worked ties;
+* the router against a hand-worked table and brute-force order checks.
 
 All run on the CPU.
 """
@@ -296,12 +297,12 @@ def test_moe_rejects_bad_expert_id(orc):
         orc.moe_matvec(Q4_K, We, 2, np.array([[0, 2]], np.int32), None, x, False, 4, 256, 1, 2)
 
 
-def test_routing_generator_is_top_k_softmax():
+def test_routing_generator_shape():
     g = synth.rng(113)
     ids, gate = synth.gen_routing(16, 128, 8, g)
     assert ids.shape == (16, 8) and gate.shape == (16, 8)
-    assert all(len(set(r)) == 8 for r in ids)
-    assert np.allclose(gate.sum(axis=1), 1.0, atol=1e-6) and np.all(np.diff(gate, axis=1) <= 0)
+    assert all(len(set(r)) == 8 for r in ids) and ids.min() >= 0 and ids.max() < 128
+    assert np.allclose(gate.sum(axis=1), 1.0, atol=1e-6) and np.all(gate > 0)
 
 
 def test_moe_group_by_definition():
@@ -348,3 +349,42 @@ def test_dequant_bf16_is_the_fp32_weights_rounded(orc, qtype):
     w = orc.dequant(qtype, blocks)
     ref = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(orc.dequant_bf16(qtype, blocks), ref)
+
+
+def test_route_hand_worked():
+    """Router pin: a hand-worked row -- equal logits in index order, -inf after
+    every finite logit, a NaN after everything -- with closed-form gates."""
+    import oracle
+    l = np.array([[1.0, 3.0, 3.0, 0.0, np.nan, -np.inf],
+                  [2.0, 2.0, 2.0, 2.0, 2.0, 2.0]], dtype=np.float32)
+    ids, gate = oracle.moe_route(l, 4)
+    assert ids.tolist() == [[1, 2, 0, 3], [0, 1, 2, 3]]
+    e = np.exp(np.array([0.0, 0.0, -2.0, -3.0]))
+    assert np.allclose(gate[0], e / e.sum(), rtol=1e-15, atol=0)
+    assert np.allclose(gate[1], 0.25, rtol=1e-15, atol=0)
+    ids5, _ = oracle.moe_route(l, 6)
+    assert ids5[0].tolist() == [1, 2, 0, 3, 5, 4]
+
+
+def test_route_brute_force_order():
+    """Every selected logit ranks at or above every unselected one, equal
+    logits are taken in index order, the gates are a softmax of the selected
+    logits (sum 1, ratios exp(l_i - l_j)); integer logits force many ties."""
+    import oracle
+    g = np.random.default_rng(116)
+    for E, k in ((128, 8), (16, 16), (300, 5)):
+        l = g.integers(-4, 5, size=(40, E)).astype(np.float32)
+        ids, gate = oracle.moe_route(l, k)
+        for m in range(40):
+            sel = list(ids[m])
+            rest = [e for e in range(E) if e not in sel]
+            vals = l[m, sel]
+            assert all(vals[i] >= vals[i + 1] for i in range(k - 1))
+            for i in range(k - 1):  # ties in index order
+                if vals[i] == vals[i + 1]:
+                    assert sel[i] < sel[i + 1]
+            if rest:
+                worst = vals[-1]
+                assert all(l[m, e] < worst or (l[m, e] == worst and e > sel[-1]) for e in rest)
+            assert abs(gate[m].sum() - 1.0) < 1e-12
+            assert np.allclose(gate[m] / gate[m][0], np.exp(vals.astype(np.float64) - vals[0]), rtol=1e-12)
