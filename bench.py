@@ -358,7 +358,7 @@ def run_workload(args):
              {"cases": res})
     elif wl == "moe":
         E, H, F, SH, top_k, layers = 128, 2816, 704, 2112, 8, 30
-        for M in (1, 16):
+        for M, rho in ((1, 0.0), (8, 0.62), (16, 0.0)):  # M = 8: a verify block's correlated routing
             g = synth.rng(2, M)
             Wg0 = synth.gen_matrix(synth.Q4_K, E * F, H, g)
             Wd0 = synth.gen_matrix(synth.Q4_K, E * H, F, g)
@@ -367,7 +367,7 @@ def run_workload(args):
                 gl = synth.rng(2, M, li)
                 lay = {"Wg": torch.from_numpy(Wg0).to(dev), "Wu": torch.from_numpy(Wg0).to(dev),
                        "Wd": torch.from_numpy(Wd0).to(dev),
-                       "logits": torch.from_numpy(synth.gen_logits(M, E, gl)).to(dev),
+                       "logits": torch.from_numpy(synth.gen_logits(M, E, gl, rho=rho)).to(dev),
                        "ids": torch.empty((M, top_k), dtype=torch.int32, device=dev),
                        "gate": torch.empty((M, top_k), dtype=torch.float32, device=dev),
                        "Sg": torch.from_numpy(synth.gen_matrix(synth.Q4_K, SH, H, gl)).to(dev),
@@ -410,19 +410,35 @@ def run_workload(args):
                         kq.kq_matvec(synth.Q4_K, L["Sg"], x, kq.KQ_BF16, ysg, SH, H, M, stream)
                         kq.kq_matvec(synth.Q4_K, L["Su"], x, kq.KQ_BF16, ysu, SH, H, M, stream)
                     kq.kq_matvec(synth.Q4_K, L["Sd"], xsh, kq.KQ_BF16, ysd, H, SH, M, stream)
-            ms = _timed_graph(torch, step, stream, args.steps, args.warmup)
+            # the layer as one expert FFN: router, gate|up + activation, down + combine + shared (3 launches)
+            wsf = kq.moe_ffn_workspace(H, F, SH, M, top_k, E)
+            yf = torch.empty((M, H), dtype=torch.float32, device=dev)
+            for L in per_layer:
+                L["ffn"] = kq.ffn_weights(synth.Q4_K, synth.Q4_K, E, kq.KQ_ACT_GELU_TANH, F, L["Wg"], L["Wu"],
+                                          L["Wd"], SH, L["Sg"], L["Su"], L["Sd"])
+
+            def step_ffn():
+                for L in per_layer:
+                    kq.kq_moe_route(L["logits"], M, E, top_k, L["ids"], L["gate"], None, stream)
+                    kq.kq_moe_ffn(L["ffn"], L["ids"], L["gate"], x, kq.KQ_BF16, yf, H, M, top_k, wsf, wsf.numel(),
+                                  stream)
+            ms_sep = _timed_graph(torch, step, stream, args.steps, args.warmup)
             kq.kq_moe_check(wsg)
             kq.kq_moe_check(wsd)
+            ms = _timed_graph(torch, step_ffn, stream, args.steps, args.warmup)
+            kq.kq_moe_check(wsf)
             route_ms = _timed_graph(torch, route_all, stream, args.steps, args.warmup)
             for L in per_layer:  # distinct experts the router picked (the expert bytes a step reads)
                 L["nexp"] = int(torch.unique(L["ids"]).numel())
             eb = synth.matrix_bytes(synth.Q4_K, F, H) * 2 + synth.matrix_bytes(synth.Q4_K, H, F)
             sb = synth.matrix_bytes(synth.Q4_K, SH, H) * 2 + synth.matrix_bytes(synth.Q4_K, H, SH)
             nbytes = sum(L["nexp"] * eb + sb for L in per_layer)
-            line(f"routed MoE decode, 30 layers, router + 128 experts top-8 + shared FFN, Q4_K, M={M}", nbytes, ms,
+            line(f"routed MoE decode, 30 layers: router + expert FFN (128 experts top-8, GELU-gated) + shared FFN, "
+                 f"Q4_K, M={M}" + (f", correlated routing (rho {rho})" if rho else ""), nbytes, ms,
                  {"tok_s_equiv": M * 1e3 / ms, "distinct_experts_per_layer": sum(L["nexp"] for L in per_layer) / layers,
-                  "launches_per_step": (6 if M == 1 else 7) * layers,
-                  "router_us_per_layer": route_ms * 1e3 / layers})
+                  "launches_per_step": 3 * layers, "router_us_per_layer": route_ms * 1e3 / layers,
+                  "separate_products": {"ms_per_step": ms_sep, "GB/s": nbytes / (ms_sep * 1e-3) / 1e9,
+                                        "launches_per_step": (6 if M == 1 else 7) * layers}})
             del per_layer
             torch.cuda.empty_cache()
     else:

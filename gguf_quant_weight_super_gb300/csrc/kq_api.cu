@@ -273,6 +273,62 @@ kq_status kq_moe_route(const float* logits, int64_t M, int32_t n_experts, int32_
   return cuda_status(e);
 }
 
+size_t kq_moe_ffn_workspace_size(int64_t H, int64_t F, int64_t SH, int64_t M, int32_t top_k, int32_t n_experts) {
+  if (H <= 0 || F <= 0 || SH < 0 || M <= 0 || top_k <= 0 || n_experts <= 0 || M * top_k > 512) return 0;
+  return ffn_layout(H, F, SH, M, top_k, n_experts).bytes;
+}
+
+kq_status kq_moe_ffn_offsets(int64_t H, int64_t F, int64_t SH, int64_t M, int32_t top_k, int32_t n_experts,
+                             size_t* h_offset, size_t* hs_offset) {
+  if (!kq_moe_ffn_workspace_size(H, F, SH, M, top_k, n_experts) || !h_offset || !hs_offset) return KQ_ERR_ARG;
+  const FfnLayout L = ffn_layout(H, F, SH, M, top_k, n_experts);
+  *h_offset = L.h_off;
+  *hs_offset = L.hs_off;
+  return KQ_OK;
+}
+
+kq_status kq_moe_ffn(const kq_moe_ffn_weights* w, const int32_t* expert_ids, const float* gate_w, const void* x,
+                     int x_dtype, float* y, int64_t H, int64_t M, int32_t top_k, void* workspace,
+                     size_t workspace_bytes, kq_stream_t stream) {
+  if (!w) return KQ_ERR_ARG;
+  if (!valid_type(w->type_gate_up) || !valid_type(w->type_down)) return KQ_ERR_TYPE;
+  if (x_dtype != KQ_F32 && x_dtype != KQ_BF16) return KQ_ERR_ARG;
+  if (w->act != KQ_ACT_SILU && w->act != KQ_ACT_GELU_TANH) return KQ_ERR_ARG;
+  if (H < 0 || w->F <= 0 || w->SH < 0 || M < 0 || top_k <= 0 || w->n_experts <= 0) return KQ_ERR_ARG;
+  if (H % 32 || w->F % 32 || w->SH % 32) return KQ_ERR_SHAPE;
+  if (H == 0 || M == 0) return KQ_OK;
+  if (!ffn_supported(w->type_gate_up, w->type_down, H, w->F, w->SH, M, top_k, w->n_experts))
+    return KQ_ERR_UNSUPPORTED;
+  if (!w->W_gate || !w->W_up || !w->W_down || !expert_ids || !gate_w || !x || !y) return KQ_ERR_ARG;
+  if (w->SH > 0 && (!w->Ws_gate || !w->Ws_up || !w->Ws_down)) return KQ_ERR_ARG;
+  if (!aligned(w->W_gate, 16) || !aligned(w->W_up, 16) || !aligned(w->W_down, 16) || !aligned(x, 16) ||
+      !aligned(y, 4) || !aligned(expert_ids, 4) || !aligned(gate_w, 4))
+    return KQ_ERR_ALIGN;
+  if (w->SH > 0 && (!aligned(w->Ws_gate, 16) || !aligned(w->Ws_up, 16) || !aligned(w->Ws_down, 16)))
+    return KQ_ERR_ALIGN;
+  if (!workspace || !aligned(workspace, 256) ||
+      workspace_bytes < ffn_layout(H, w->F, w->SH, M, top_k, w->n_experts).bytes)
+    return KQ_ERR_WORKSPACE;
+  FfnWeights fw;
+  fw.type_gu = w->type_gate_up;
+  fw.type_dn = w->type_down;
+  fw.n_experts = w->n_experts;
+  fw.act = w->act;
+  fw.F = w->F;
+  fw.SH = w->SH;
+  fw.W_gate = w->W_gate;
+  fw.W_up = w->W_up;
+  fw.W_down = w->W_down;
+  fw.Ws_gate = w->Ws_gate;
+  fw.Ws_up = w->Ws_up;
+  fw.Ws_down = w->Ws_down;
+  cudaError_t e = launch_moe_ffn(fw, expert_ids, gate_w, x, x_dtype == KQ_BF16, y, H, static_cast<int>(M), top_k,
+                                 workspace, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return KQ_ERR_UNSUPPORTED;
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_status(e);
+}
+
 kq_status kq_moe_check(void* workspace, kq_stream_t stream) {
   if (!workspace) return KQ_ERR_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -82,6 +82,21 @@ cudaError_t launch_moe_static(int qtype, const void* W, int n_experts, const int
                               const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M,
                               int top_k, cudaStream_t st);
 
+// Expert FFN of a layer (kq_moe.cu): gate|up + activation, then down + gated combine.
+struct FfnWeights {
+  int type_gu, type_dn, n_experts, act;
+  int64_t F, SH;
+  const void *W_gate, *W_up, *W_down, *Ws_gate, *Ws_up, *Ws_down;
+};
+struct FfnLayout {
+  int Dmax;
+  size_t plan_off, cnt_off, part_off, h_off, hs_off, sp_off, bytes;
+};
+FfnLayout ffn_layout(int64_t H, int64_t F, int64_t SH, int64_t M, int top_k, int n_experts);
+bool ffn_supported(int type_gu, int type_dn, int64_t H, int64_t F, int64_t SH, int64_t M, int top_k, int n_experts);
+cudaError_t launch_moe_ffn(const FfnWeights& fw, const int32_t* ids, const float* gate, const void* x, int x_bf16,
+                           float* y, int64_t H, int M, int top_k, void* ws, cudaStream_t st);
+
 // MoE router (kq_route.cu): top-k + softmax over the selected logits, and the
 // grouping plan (written at ws + 256 in kq_moe_matvec's layout when ws is set)
 bool route_supported(int64_t M, int E, int top_k);

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(PKG, "libkq.so")
 
 KQ_Q4_K, KQ_Q5_K, KQ_Q6_K = 1, 2, 3
 KQ_F32, KQ_BF16 = 0, 1
+KQ_ACT_SILU, KQ_ACT_GELU_TANH = 0, 1
 KQ_OK = 0
 STATUS = {0: "KQ_OK", -1: "KQ_ERR_ARG", -2: "KQ_ERR_TYPE", -3: "KQ_ERR_SHAPE", -4: "KQ_ERR_UNSUPPORTED",
           -5: "KQ_ERR_ALIGN", -6: "KQ_ERR_CUDA", -7: "KQ_ERR_WORKSPACE", -8: "KQ_ERR_DEVICE"}
@@ -37,6 +38,10 @@ SIGNATURES = {
     "kq_moe_matvec": (_I, [_I, _P, ctypes.c_int32, _P, _P, _P, _I, _I, _P, _I64, _I64, _I64, ctypes.c_int32,
                            _P, _SZ, _P]),
     "kq_moe_check": (_I, [_P, _P]),
+    "kq_moe_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32]),
+    "kq_moe_ffn_offsets": (_I, [_I64, _I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32,
+                                ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]),
+    "kq_moe_ffn": (_I, [_P, _P, _P, _P, _I, _P, _I64, _I64, ctypes.c_int32, _P, _SZ, _P]),
     "kq_moe_matvec_noalloc": (_I, [_I, _P, ctypes.c_int32, _P, _P, _P, _I, _I, _P, _I64, _I64, _I64,
                                    ctypes.c_int32, _P]),
     "kq_device_error": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
@@ -222,6 +227,47 @@ def moe_workspace(N, M, top_k, n_experts, device="cuda") -> torch.Tensor:
     if n == 0:
         raise KQError("kq_moe_workspace_size", -4)
     return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+class KqMoeFfnWeights(ctypes.Structure):
+    """struct kq_moe_ffn_weights of include/kq.h."""
+    _fields_ = [("type_gate_up", ctypes.c_int32), ("type_down", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("act", ctypes.c_int32), ("F", ctypes.c_int64), ("SH", ctypes.c_int64),
+                ("W_gate", ctypes.c_void_p), ("W_up", ctypes.c_void_p), ("W_down", ctypes.c_void_p),
+                ("Ws_gate", ctypes.c_void_p), ("Ws_up", ctypes.c_void_p), ("Ws_down", ctypes.c_void_p)]
+
+
+def ffn_weights(type_gate_up, type_down, n_experts, act, F, W_gate, W_up, W_down, SH=0, Ws_gate=None, Ws_up=None,
+                Ws_down=None) -> KqMoeFfnWeights:
+    return KqMoeFfnWeights(type_gate_up, type_down, n_experts, act, F, SH, _ptr(W_gate), _ptr(W_up), _ptr(W_down),
+                           _ptr(Ws_gate), _ptr(Ws_up), _ptr(Ws_down))
+
+
+def kq_moe_ffn_workspace_size(H, F, SH, M, top_k, n_experts) -> int:
+    return lib().kq_moe_ffn_workspace_size(H, F, SH, M, top_k, n_experts)
+
+
+def kq_moe_ffn_offsets(H, F, SH, M, top_k, n_experts):
+    """(byte offset of h [M*top_k][F], byte offset of hs [M][SH]) in the workspace."""
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("kq_moe_ffn_offsets", lib().kq_moe_ffn_offsets(H, F, SH, M, top_k, n_experts, ctypes.byref(a),
+                                                          ctypes.byref(b)))
+    return a.value, b.value
+
+
+def moe_ffn_workspace(H, F, SH, M, top_k, n_experts, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace tensor for kq_moe_ffn."""
+    n = kq_moe_ffn_workspace_size(H, F, SH, M, top_k, n_experts)
+    if n == 0:
+        raise KQError("kq_moe_ffn_workspace_size", -4)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def kq_moe_ffn(weights: KqMoeFfnWeights, expert_ids, gate_w, x, x_dtype, y, H, M, top_k, workspace,
+               workspace_bytes, stream=None):
+    _check("kq_moe_ffn", lib().kq_moe_ffn(ctypes.cast(ctypes.pointer(weights), ctypes.c_void_p), _ptr(expert_ids),
+                                          _ptr(gate_w), _ptr(x), x_dtype, _ptr(y), H, M, top_k, _ptr(workspace),
+                                          workspace_bytes, _stream(stream)))
 
 
 def kq_device_error(clear: bool = False) -> int:

@@ -102,11 +102,17 @@ def gen_routing(M: int, n_experts: int, top_k: int, g: np.random.Generator):
     return ids, gate
 
 
-def gen_logits(M: int, n_experts: int, g: np.random.Generator, ties: bool = False) -> np.ndarray:
+def gen_logits(M: int, n_experts: int, g: np.random.Generator, ties: bool = False, rho: float = 0.0) -> np.ndarray:
     """Router logits [M, n_experts] fp32: N(0, 1), or small integers (-4..4)
-    so that equal logits are common."""
+    so that equal logits are common.  rho > 0 correlates the tokens (as
+    neighbouring tokens of a verify block are): sqrt(rho) z + sqrt(1 - rho) z_m
+    with one N(0, 1) draw z shared by all tokens; rho = 0.62 makes 8 tokens'
+    top-8 of 128 cover about 29 distinct experts."""
     if ties:
         return g.integers(-4, 5, size=(M, n_experts)).astype(np.float32)
+    if rho > 0.0:
+        z = g.standard_normal(n_experts)
+        return (np.sqrt(rho) * z + np.sqrt(1.0 - rho) * g.standard_normal((M, n_experts))).astype(np.float32)
     return g.standard_normal((M, n_experts), dtype=np.float32)
 
 

@@ -279,6 +279,61 @@ kq_status kq_moe_route(const float *logits, int64_t M, int32_t n_experts, int32_
                        float *gate_w, void *workspace, size_t workspace_bytes, kq_stream_t stream);
 
 /*
+ * The expert FFN of one MoE layer: routed experts plus an optional shared
+ * expert, gate|up -> activation -> down -> gate-weighted combine.
+ *
+ * "ANE Fieldfare" README, "How it works": each layer runs a shared FFN that
+ * every token goes through plus the 8 routed experts it picked, each a small
+ * feed-forward block.  The pages give neither the activation nor the order of
+ * the final sums; this library takes the gated form
+ *   h_j  = act(W_gate[e_j] x) * (W_up[e_j] x)        (e_j = expert_ids[m][j])
+ *   hs   = act(Ws_gate x) * (Ws_up x)
+ *   y[m] = sum_j gate_w[m][j] * (W_down[e_j] h_j)  +  Ws_down hs
+ * with the routed terms added in slot order and the shared term last, all in
+ * fp32 (h kept in fp32).  act is a parameter:
+ *   KQ_ACT_SILU       g / (1 + exp(-g))
+ *   KQ_ACT_GELU_TANH  0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3)))
+ *
+ * Weights (device, 16-byte aligned, same block layout as kq_matvec):
+ *   W_gate, W_up  [n_experts][F][H/256 blocks] of type_gate_up
+ *   W_down        [n_experts][H][F/256 blocks] of type_down
+ *   Ws_gate, Ws_up [SH][H/256 blocks] (type_gate_up), Ws_down [H][SH/256 blocks]
+ *                 (type_down); all NULL and SH = 0 for no shared expert.
+ * x [M][H] fp32 or bf16 (16-byte aligned); y [M][H] fp32; expert_ids, gate_w
+ * [M][top_k] (an id outside [0, n_experts) drops its pair and sets the
+ * workspace error word, read by kq_moe_check).
+ * Two launches on stream (programmatic dependent launch); the workspace
+ * (kq_moe_ffn_workspace_size bytes, 256-byte aligned, zero-filled once before
+ * first use) holds the error word, the grouping plan at byte 256 (as in
+ * kq_moe_matvec), arrival counters (back at zero after each call) and the fp32
+ * intermediates; h [M*top_k][F] and hs [M][SH] start at the offsets
+ * kq_moe_ffn_offsets returns (for inspection).
+ * Errors: KQ_ERR_ARG, KQ_ERR_TYPE, KQ_ERR_SHAPE (H, F or SH not a multiple of
+ * 32), KQ_ERR_UNSUPPORTED (M*top_k > 512, n_experts > 4096, a K above 16384 or
+ * rows too wide for a 100 KB tile), KQ_ERR_ALIGN, KQ_ERR_WORKSPACE.
+ */
+#define KQ_ACT_SILU 0
+#define KQ_ACT_GELU_TANH 1
+
+typedef struct kq_moe_ffn_weights {
+  int32_t type_gate_up; /* block type of W_gate, W_up, Ws_gate, Ws_up */
+  int32_t type_down;    /* block type of W_down, Ws_down              */
+  int32_t n_experts;
+  int32_t act;          /* KQ_ACT_SILU or KQ_ACT_GELU_TANH            */
+  int64_t F;            /* routed expert width                        */
+  int64_t SH;           /* shared expert width, 0 = none              */
+  const void *W_gate, *W_up, *W_down;
+  const void *Ws_gate, *Ws_up, *Ws_down;
+} kq_moe_ffn_weights;
+
+size_t kq_moe_ffn_workspace_size(int64_t H, int64_t F, int64_t SH, int64_t M, int32_t top_k, int32_t n_experts);
+kq_status kq_moe_ffn_offsets(int64_t H, int64_t F, int64_t SH, int64_t M, int32_t top_k, int32_t n_experts,
+                             size_t *h_offset, size_t *hs_offset);
+kq_status kq_moe_ffn(const kq_moe_ffn_weights *w, const int32_t *expert_ids, const float *gate_w, const void *x,
+                     int x_dtype, float *y, int64_t H, int64_t M, int32_t top_k, void *workspace,
+                     size_t workspace_bytes, kq_stream_t stream);
+
+/*
  * Read the device error word (KQ_OK when clean); with clear != 0 also reset
  * it.  Synchronizes the device.
  */

@@ -71,6 +71,7 @@ def bind(path: str):
     L.oracle_pack.argtypes = [I, ctypes.POINTER(_Fields), P]
     L.oracle_dequant_block_f64.argtypes = [I, P, P]
     L.oracle_dequant.argtypes = [I, P, I64, P]
+    L.oracle_dequant_f64.argtypes = [I, P, I64, P]
     L.oracle_matvec.argtypes = [I, P, I64, I64, P, I, I64, P, P, I]
     L.oracle_moe_matvec.argtypes = [I, P, I, P, P, P, I, I, I64, I64, I64, I, P, P, I]
     return L
@@ -131,6 +132,16 @@ def dequant(qtype: int, blocks: np.ndarray) -> np.ndarray:
     assert nb * BLOCK_BYTES[qtype] == raw.size
     out = np.zeros(nb * 256, dtype=np.float32)
     assert lib().oracle_dequant(qtype, _ptr(raw), nb, _ptr(out)) == 0
+    return out
+
+
+def dequant_f64(qtype: int, blocks: np.ndarray) -> np.ndarray:
+    """All blocks -> their exact weights in fp64 (before any fp32 rounding)."""
+    raw = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1)
+    nb = raw.size // BLOCK_BYTES[qtype]
+    assert nb * BLOCK_BYTES[qtype] == raw.size
+    out = np.zeros(nb * 256, dtype=np.float64)
+    assert lib().oracle_dequant_f64(qtype, _ptr(raw), nb, _ptr(out)) == 0
     return out
 
 
@@ -235,3 +246,78 @@ def moe_group(ids: np.ndarray, n_experts: int):
         pairs.extend(i for i, v in enumerate(flat) if v == e)
     offsets.append(len(pairs))
     return experts, offsets, pairs
+
+
+def ffn_act(act: int, g: np.ndarray) -> np.ndarray:
+    """The FFN activations by definition, fp64: 0 = SiLU g / (1 + e^-g);
+    1 = GELU in its tanh form, 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3)))."""
+    g = np.asarray(g, dtype=np.float64)
+    if act == 1:
+        return 0.5 * g * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (g + 0.044715 * g ** 3)))
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+def _x_f64(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:  # bfloat16 bits: the high half of an fp32
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def _matrix_f64(qtype: int, W: np.ndarray, row0: int, N: int, K: int) -> np.ndarray:
+    """Rows row0 .. row0+N of a block matrix with K columns, as fp64 [N, K]."""
+    nb = (K + 255) // 256
+    rb = nb * BLOCK_BYTES[qtype]
+    raw = np.ascontiguousarray(W, dtype=np.uint8).reshape(-1)[row0 * rb:(row0 + N) * rb]
+    return dequant_f64(qtype, raw).reshape(N, nb * 256)[:, :K]
+
+
+def moe_ffn(type_gu: int, W_gate, W_up, type_dn: int, W_down, n_experts: int, ids, gate, x, act: int,
+            H: int, F: int, M: int, top_k: int, shared=None):
+    """The expert FFN of one MoE layer by its definition (fp64, numpy matmul on
+    the exact weights, as every product here uses them).
+
+    "ANE Fieldfare" README, "How it works": a shared FFN every token goes
+    through plus the routed experts each token picked.  Reading: gated FFN
+    blocks, h = act(W_gate x) * (W_up x), y = sum_j g_j W_down[e_j] h_j + shared.
+    shared = (Ws_gate, Ws_up, Ws_down, SH) or None.  Ids outside
+    [0, n_experts) are dropped.  Returns a dict: y, s (sum of |g_j| |W_down| |h_j|
+    plus the shared |Ws_down| |hs|), h, g, u [M*top_k, F] (NaN for dropped
+    pairs: h and the gate and up products), sg, su (their |W| |x| sums), and
+    hs, gs, us, sgs, sus for the shared expert."""
+    ids = np.asarray(ids, dtype=np.int64).reshape(M, top_k)
+    gate = np.asarray(gate, dtype=np.float32).astype(np.float64).reshape(M, top_k)
+    X = _x_f64(x).reshape(M, H)
+    AX = np.abs(X)
+    MK = M * top_k
+    out = {"y": np.zeros((M, H)), "s": np.zeros((M, H)), "h": np.full((MK, F), np.nan),
+           "g": np.full((MK, F), np.nan), "u": np.full((MK, F), np.nan),
+           "sg": np.zeros((MK, F)), "su": np.zeros((MK, F))}
+    for e in sorted({int(v) for v in ids.reshape(-1) if 0 <= v < n_experts}):
+        pairs = [i for i in range(MK) if ids.reshape(-1)[i] == e]
+        ms = [p // top_k for p in pairs]
+        Wg = _matrix_f64(type_gu, W_gate, e * F, F, H)
+        Wu = _matrix_f64(type_gu, W_up, e * F, F, H)
+        g, u = X[ms] @ Wg.T, X[ms] @ Wu.T
+        h = ffn_act(act, g) * u
+        out["h"][pairs], out["g"][pairs], out["u"][pairs] = h, g, u
+        out["sg"][pairs], out["su"][pairs] = AX[ms] @ np.abs(Wg).T, AX[ms] @ np.abs(Wu).T
+        del Wg, Wu
+        Wd = _matrix_f64(type_dn, W_down, e * H, H, F)
+        d, sd = h @ Wd.T, np.abs(h) @ np.abs(Wd).T
+        for k, p in enumerate(pairs):
+            m, j = divmod(p, top_k)
+            out["y"][m] += gate[m, j] * d[k]
+            out["s"][m] += abs(gate[m, j]) * sd[k]
+    if shared is not None:
+        Wsg, Wsu, Wsd, SH = shared
+        A = _matrix_f64(type_gu, Wsg, 0, SH, H)
+        B = _matrix_f64(type_gu, Wsu, 0, SH, H)
+        g, u = X @ A.T, X @ B.T
+        hs = ffn_act(act, g) * u
+        out.update(hs=hs, gs=g, us=u, sgs=AX @ np.abs(A).T, sus=AX @ np.abs(B).T)
+        Cd = _matrix_f64(type_dn, Wsd, 0, H, SH)
+        out["y"] += hs @ Cd.T
+        out["s"] += np.abs(hs) @ np.abs(Cd).T
+    return out

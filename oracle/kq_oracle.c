@@ -202,6 +202,16 @@ int oracle_dequant(int type, const uint8_t *blocks, int64_t n_blocks, float *out
     return 0;
 }
 
+/* All blocks -> their exact weights in fp64 (the values every product uses). */
+int oracle_dequant_f64(int type, const uint8_t *blocks, int64_t n_blocks, double *out)
+{
+    int nbytes = oracle_block_bytes(type);
+    if (!nbytes || n_blocks < 0) return -1;
+    for (int64_t b = 0; b < n_blocks; ++b)
+        oracle_dequant_block_f64(type, blocks + b * nbytes, out + b * 256);
+    return 0;
+}
+
 static double x_value(const void *x, int x_dtype, int64_t idx)
 {
     if (x_dtype == ORACLE_X_BF16) return oracle_bf16_to_double(((const uint16_t *)x)[idx]);

@@ -108,6 +108,35 @@ def test_route_argument_errors_without_gpu(L):
     assert r(fake, 4, 128, 8, fake, fake, fake, 64, None) == -7        # workspace too small
 
 
+def test_ffn_argument_errors_without_gpu(L):
+    f = 0x1000
+    def call(w, ids=f, gate=f, x=f, xd=0, y=f, H=512, M=2, k=4, ws=f, wsb=1 << 30):
+        return kq.lib().kq_moe_ffn(None if w is None else ctypes.cast(ctypes.pointer(w), ctypes.c_void_p),
+                                   ids, gate, x, xd, y, H, M, k, ws, wsb, None)
+    def w(**kw):
+        a = dict(type_gate_up=1, type_down=3, n_experts=16, act=1, F=320, W_gate=f, W_up=f, W_down=f, SH=0)
+        a.update(kw)
+        return kq.ffn_weights(a["type_gate_up"], a["type_down"], a["n_experts"], a["act"], a["F"], a["W_gate"],
+                              a["W_up"], a["W_down"], a["SH"], a.get("Ws_gate"), a.get("Ws_up"), a.get("Ws_down"))
+    assert call(None) == -1                                  # no weights struct
+    assert call(w(type_down=9)) == -2                        # unknown block type
+    assert call(w(act=7)) == -1                              # unknown activation
+    assert call(w(), xd=5) == -1                             # bad x dtype
+    assert call(w(F=100)) == -3                              # F not a multiple of 32
+    assert call(w(), H=500) == -3                            # H not a multiple of 32
+    assert call(w(), M=0) == 0                               # empty: no-op
+    assert call(w(), M=200, k=4) == -4                       # 800 pairs > 512
+    assert call(w(SH=64)) == -1                              # shared width without shared weights
+    assert call(w(W_up=None)) == -1                          # null weight
+    assert call(w(W_gate=0x1008)) == -5                      # weight alignment
+    assert call(w(), ws=0x1080) == -7                        # workspace alignment
+    assert call(w(), wsb=64) == -7                           # workspace too small
+    assert kq.kq_moe_ffn_workspace_size(512, 320, 0, 2, 4, 16) > 0
+    assert kq.kq_moe_ffn_workspace_size(512, 320, 0, 200, 4, 16) == 0
+    h_off, hs_off = kq.kq_moe_ffn_offsets(512, 320, 288, 2, 4, 16)
+    assert h_off % 256 == 0 and hs_off >= h_off + 4 * 8 * 320
+
+
 def test_moe_argument_errors_without_gpu(L):
     f = 0x100000
     def call(**kw):

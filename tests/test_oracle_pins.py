@@ -388,3 +388,133 @@ def test_route_brute_force_order():
                 assert all(l[m, e] < worst or (l[m, e] == worst and e > sel[-1]) for e in rest)
             assert abs(gate[m].sum() - 1.0) < 1e-12
             assert np.allclose(gate[m] / gate[m][0], np.exp(vals.astype(np.float64) - vals[0]), rtol=1e-12)
+
+
+def test_ffn_activations():
+    """Activation pins: SiLU at closed-form points; the tanh form of GELU
+    within 5e-4 of the erf form (its known approximation error, 4.7e-4 at
+    most) over [-8, 8]; both satisfy act(x) - act(-x) = x, act(0) = 0, and
+    tend to x for large x and to 0 for very negative x."""
+    import math
+    import oracle
+    assert abs(oracle.ffn_act(0, np.array([1.0]))[0] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    assert abs(oracle.ffn_act(0, np.array([math.log(3.0)]))[0] - 0.75 * math.log(3.0)) < 1e-15  # sigma(ln 3) = 3/4
+    x = np.linspace(-8, 8, 20001)
+    erf_gelu = np.array([0.5 * v * (1 + math.erf(v / math.sqrt(2))) for v in x])
+    assert np.max(np.abs(oracle.ffn_act(1, x) - erf_gelu)) < 5e-4
+    for act in (0, 1):
+        a = oracle.ffn_act(act, x)
+        assert np.allclose(a - oracle.ffn_act(act, -x), x, rtol=0, atol=1e-12)
+        assert oracle.ffn_act(act, np.array([0.0]))[0] == 0.0
+        assert abs(oracle.ffn_act(act, np.array([40.0]))[0] - 40.0) < 1e-12
+        assert abs(oracle.ffn_act(act, np.array([-40.0]))[0]) < 1e-12
+
+
+def _ffn_case(seed, E=4, H=512, F=96, SH=64, M=3, top_k=2, qg=Q4_K, qd=Q6_K):
+    g = synth.rng(seed)
+    Wg = synth.gen_matrix(qg, E * F, H, g)
+    Wu = synth.gen_matrix(qg, E * F, H, g)
+    Wd = synth.gen_matrix(qd, E * H, F, g)
+    sh = (synth.gen_matrix(qg, SH, H, g), synth.gen_matrix(qg, SH, H, g), synth.gen_matrix(qd, H, SH, g), SH)
+    ids, gate = synth.gen_routing(M, E, top_k, g)
+    x = synth.gen_x(M, H, g)
+    return dict(Wg=Wg, Wu=Wu, Wd=Wd, sh=sh, ids=ids, gate=gate, x=x, E=E, H=H, F=F, M=M, top_k=top_k, qg=qg, qd=qd)
+
+
+def test_moe_ffn_matches_composed_dense_products():
+    """FFN pin: the oracle's layer (numpy matmul on dequantized weights)
+    against the same layer composed from the C dense product oracle.matvec
+    (its own decode and loops): gate and up per pair, the activation, down
+    with h rounded to fp32, the gated sum and the shared term."""
+    import oracle
+    c = _ffn_case(131)
+    E, H, F, M, k = c["E"], c["H"], c["F"], c["M"], c["top_k"]
+    for act in (0, 1):
+        r = oracle.moe_ffn(c["qg"], c["Wg"], c["Wu"], c["qd"], c["Wd"], E, c["ids"], c["gate"], c["x"], act,
+                           H, F, M, k, shared=c["sh"])
+        rb_g = synth.matrix_bytes(c["qg"], F, H)
+        rb_d = synth.matrix_bytes(c["qd"], H, F)
+        y = np.zeros((M, H))
+        for m in range(M):
+            for j in range(k):
+                e = int(c["ids"][m, j])
+                gg, _ = oracle.matvec(c["qg"], c["Wg"][e * rb_g:(e + 1) * rb_g], F, H, c["x"][m:m + 1])
+                uu, _ = oracle.matvec(c["qg"], c["Wu"][e * rb_g:(e + 1) * rb_g], F, H, c["x"][m:m + 1])
+                h = oracle.ffn_act(act, gg) * uu
+                p = m * k + j  # the two sum orders differ by fp64 rounding, relative to sum |w x|
+                bound = 1e-12 * (1.2 * np.abs(uu[0]) * r["sg"][p] + np.abs(oracle.ffn_act(act, gg[0])) * r["su"][p])
+                assert np.all(np.abs(h[0] - r["h"][p]) <= bound)
+                dd, _ = oracle.matvec(c["qd"], c["Wd"][e * rb_d:(e + 1) * rb_d], H, F, h.astype(np.float32))
+                y[m] += np.float64(c["gate"][m, j]) * dd[0]
+            Wsg, Wsu, Wsd, SH = c["sh"]
+            gs, _ = oracle.matvec(c["qg"], Wsg, SH, H, c["x"][m:m + 1])
+            us, _ = oracle.matvec(c["qg"], Wsu, SH, H, c["x"][m:m + 1])
+            hs = oracle.ffn_act(act, gs) * us
+            ds, _ = oracle.matvec(c["qd"], Wsd, H, SH, hs.astype(np.float32))
+            y[m] += ds[0]
+        assert np.all(np.abs(y - r["y"]) <= 1e-6 * r["s"])
+
+
+def test_moe_ffn_brute_force_tiny():
+    """FFN pin on a tiny layer with pure-Python loops over the per-block
+    exact weights (one routed slot with its gate, no shared expert)."""
+    import oracle
+    c = _ffn_case(132, E=2, H=256, F=32, M=1, top_k=1)
+    r = oracle.moe_ffn(c["qg"], c["Wg"], c["Wu"], c["qd"], c["Wd"], 2, c["ids"], c["gate"], c["x"], 1,
+                       256, 32, 1, 1)
+    e = int(c["ids"][0, 0])
+    wg = np.array([oracle.dequant_block_f64(c["qg"], b) for b in c["Wg"].reshape(-1, 144)]).reshape(2, 32, 256)[e]
+    wu = np.array([oracle.dequant_block_f64(c["qg"], b) for b in c["Wu"].reshape(-1, 144)]).reshape(2, 32, 256)[e]
+    wd = np.array([oracle.dequant_block_f64(c["qd"], b) for b in c["Wd"].reshape(-1, 210)]).reshape(2, 256, 256)[e]
+    wd = wd[:, :32]
+    xs = [float(v) for v in c["x"][0]]
+    import math
+    h = []
+    for f in range(32):
+        gv = sum(float(wg[f, k]) * xs[k] for k in range(256))
+        uv = sum(float(wu[f, k]) * xs[k] for k in range(256))
+        h.append(0.5 * gv * (1 + math.tanh(math.sqrt(2 / math.pi) * (gv + 0.044715 * gv ** 3))) * uv)
+    for n in (0, 17, 255):
+        yv = float(c["gate"][0, 0]) * sum(float(wd[n, f]) * h[f] for f in range(32))
+        assert abs(yv - r["y"][0, n]) <= 1e-12 * r["s"][0, n]
+
+
+def test_moe_ffn_invariants():
+    """Gate linearity (the routed part doubles with the gates), slot order
+    (a consistent permutation of each token's slots changes nothing), dropped
+    ids (an id out of range equals a zero gate), and no valid id (only the
+    shared term remains)."""
+    import oracle
+    c = _ffn_case(133, M=4, top_k=3)
+    args = (c["qg"], c["Wg"], c["Wu"], c["qd"], c["Wd"], c["E"])
+    dims = (c["H"], c["F"], c["M"], c["top_k"])
+    base = oracle.moe_ffn(*args, c["ids"], c["gate"], c["x"], 0, *dims, shared=c["sh"])
+    none = oracle.moe_ffn(*args, np.full_like(c["ids"], -1), c["gate"], c["x"], 0, *dims, shared=c["sh"])
+    dbl = oracle.moe_ffn(*args, c["ids"], 2 * c["gate"], c["x"], 0, *dims, shared=c["sh"])
+    assert np.allclose(dbl["y"] - none["y"], 2 * (base["y"] - none["y"]), rtol=0, atol=1e-12 * base["s"].max())
+    perm = np.array([2, 0, 1])
+    pr = oracle.moe_ffn(*args, c["ids"][:, perm], c["gate"][:, perm], c["x"], 0, *dims, shared=c["sh"])
+    assert np.allclose(pr["y"], base["y"], rtol=0, atol=1e-12 * base["s"].max())
+    ids2, g2 = c["ids"].copy(), c["gate"].copy()
+    ids2[1, 2] = c["E"] + 5
+    g2[1, 2] = 0.0
+    dropped = oracle.moe_ffn(*args, ids2, c["gate"], c["x"], 0, *dims, shared=c["sh"])
+    zero_gate = oracle.moe_ffn(*args, c["ids"], g2, c["x"], 0, *dims, shared=c["sh"])
+    assert np.allclose(dropped["y"], zero_gate["y"], rtol=0, atol=1e-12 * base["s"].max())
+    Wsg, Wsu, Wsd, SH = c["sh"]
+    gs, _ = oracle.matvec(c["qg"], Wsg, SH, c["H"], c["x"])
+    us, _ = oracle.matvec(c["qg"], Wsu, SH, c["H"], c["x"])
+    assert np.allclose(none["hs"], oracle.ffn_act(0, gs) * us, rtol=1e-12, atol=0)
+
+
+def test_dequant_f64_is_exact_weights():
+    """dequant_f64 equals the per-block exact weights, and rounded to fp32 it
+    equals dequant (the fp32 weights are the exact ones rounded once)."""
+    import oracle
+    g = synth.rng(134)
+    for qt in (Q4_K, Q5_K, Q6_K):
+        blocks = synth.gen_blocks(qt, 40, g)
+        w = oracle.dequant_f64(qt, blocks)
+        ref = np.concatenate([oracle.dequant_block_f64(qt, b) for b in blocks.reshape(40, -1)])
+        assert np.array_equal(w, ref)
+        assert np.array_equal(w.astype(np.float32), oracle.dequant(qt, blocks))
