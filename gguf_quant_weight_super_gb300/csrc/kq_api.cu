@@ -108,7 +108,7 @@ kq_status kq_matvec(int type, const void* W, const void* x, int x_dtype, float* 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int bf16 = (x_dtype == KQ_BF16);
   cudaError_t e = cudaErrorNotSupported;
-  if (M == 1 || (M == 2 && bf16)) e = launch_matvec1(type, W, x, bf16, y, N, static_cast<int>(K), st, true, M);
+  if (M == 1 || (M <= 4 && bf16)) e = launch_matvec1(type, W, x, bf16, y, N, static_cast<int>(K), st, true, M);
   if (e == cudaErrorNotSupported && bf16 && tc_supported(type, N, static_cast<int>(K), static_cast<int>(M)))
     e = launch_tc(type, W, x, y, N, static_cast<int>(K), static_cast<int>(M), st, true);
   if (e == cudaErrorNotSupported)

@@ -1,4 +1,4 @@
-// kq_gemv.cu -- one-token products y = W x (M = 1; also M = 2 with bf16 x)
+// kq_gemv.cu -- one-token products y = W x (M = 1; also M = 2..4 with bf16 x)
 // against Q4_K / Q5_K / Q6_K rows: a single matrix, or a program of matrices
 // run by one persistent launch.
 //
@@ -69,7 +69,7 @@ constexpr int NTH = NTHC + 32;         // + one producer warp
 constexpr int RING_MAX = 8;                // ring slots at most
 constexpr int CONSUMER_BAR = 1;        // named barrier of the consumer warps
 constexpr int MAX_NB = 64;             // K <= 16384
-constexpr int kMaxTokens1 = 2;         // tokens of one single-product launch (bf16 x when more than one)
+constexpr int kMaxTokens1 = 4;         // tokens of one single-product launch (bf16 x when more than one)
 // Largest stage (32 row segments): 48 KB keeps a ring of at least 4 slots.
 constexpr int64_t kSlotCap = 48 * 1024;
 // Largest stage of whole rows (one bulk copy), by rows per quad: a taller
@@ -761,11 +761,17 @@ cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, 
   a.nl_max = x_bf16 ? 2 : 3;
   a.barrier = nullptr;
   a.err = device_error_ptr();
-  if (M == 2) {  // two tokens: bf16 x only (the x slices of both tokens stay in registers)
-    switch (qtype) {
-      case T_Q4_K: return launch_single_r<T_Q4_K, 2, 2>(o.R, a, g, stream, pdl);
-      case T_Q5_K: return launch_single_r<T_Q5_K, 2, 2>(o.R, a, g, stream, pdl);
-      case T_Q6_K: return launch_single_r<T_Q6_K, 2, 2>(o.R, a, g, stream, pdl);
+  if (M > 1) {  // several tokens: bf16 x only (the x slices of all tokens stay in registers)
+    switch (qtype * 8 + M) {
+      case T_Q4_K * 8 + 2: return launch_single_r<T_Q4_K, 2, 2>(o.R, a, g, stream, pdl);
+      case T_Q5_K * 8 + 2: return launch_single_r<T_Q5_K, 2, 2>(o.R, a, g, stream, pdl);
+      case T_Q6_K * 8 + 2: return launch_single_r<T_Q6_K, 2, 2>(o.R, a, g, stream, pdl);
+      case T_Q4_K * 8 + 3: return launch_single_r<T_Q4_K, 2, 3>(o.R, a, g, stream, pdl);
+      case T_Q5_K * 8 + 3: return launch_single_r<T_Q5_K, 2, 3>(o.R, a, g, stream, pdl);
+      case T_Q6_K * 8 + 3: return launch_single_r<T_Q6_K, 2, 3>(o.R, a, g, stream, pdl);
+      case T_Q4_K * 8 + 4: return launch_single_r<T_Q4_K, 2, 4>(o.R, a, g, stream, pdl);
+      case T_Q5_K * 8 + 4: return launch_single_r<T_Q5_K, 2, 4>(o.R, a, g, stream, pdl);
+      case T_Q6_K * 8 + 4: return launch_single_r<T_Q6_K, 2, 4>(o.R, a, g, stream, pdl);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -117,8 +117,10 @@ kq_status kq_dequant_bf16(int type, const void *blocks, uint16_t *out, int64_t n
  *   x_dtype KQ_F32 or KQ_BF16; M in 1..16; K a multiple of 32.
  * Accumulation is fp32 in a fixed order, so repeated calls give identical y;
  * the order (hence the last bits of y) differs between paths: M = 1, and
- * M = 2 with bf16 x (exact integer dots per block); M = 3..16 with bf16 x
- * (tensor cores, weights rounded to bf16); M >= 2 with fp32 x.
+ * M = 2..4 with bf16 x when M x images fit beside the weight ring in shared
+ * memory (exact integer dots per block; each row then equals that token's
+ * M = 1 product bit for bit); otherwise M = 2..16 with bf16 x on the tensor
+ * cores (weights rounded to bf16); M >= 2 with fp32 x on the CUDA cores.
  */
 kq_status kq_matvec(int type, const void *W, const void *x, int x_dtype, float *y, int64_t N, int64_t K,
                     int64_t M, kq_stream_t stream);

@@ -233,27 +233,32 @@ def test_matvec_m16_ragged(qtype, NK):
 
 
 @pytest.mark.parametrize("qtype", TYPES)
-@pytest.mark.parametrize("NK", [(300, 2816), (4096, 4096), (2560, 9728)])
-def test_matvec_two_tokens_bit_identical_to_one(qtype, NK):
-    """Two tokens (bf16 x) run the one-token arithmetic on two x images: each
-    row of the pair equals that token's one-token product bit for bit (the
-    property the ANE page tests for its few-token kernel)."""
+@pytest.mark.parametrize("NK", [(300, 2816), (4096, 4096), (2560, 9728), (14336, 4096), (1024, 2560)])
+@pytest.mark.parametrize("M", [2, 3, 4])
+def test_matvec_few_tokens_bit_identical_to_one(qtype, NK, M):
+    """Two to four tokens (bf16 x) run the one-token arithmetic on M x images:
+    each row equals that token's one-token product bit for bit (the property
+    the ANE page tests for its kernel of up to 4 tokens).  Four tokens at
+    K = 9728 do not fit beside the weight ring and go to the tensor cores."""
     N, K = NK
+    if M == 4 and K > 4096:
+        pytest.skip("four x images of K = 9728 do not fit: tensor-core path")
     g = synth.rng(212, qtype, N, K)
     W = dev(synth.gen_matrix(qtype, N, K, g))
-    x = x_dev(synth.gen_x(2, K, g, "bf16"))
-    y2 = kq.matvec(qtype, W, x, N, K)
-    for m in range(2):
-        assert torch.equal(y2[m], kq.matvec(qtype, W, x[m:m + 1], N, K)[0]), m
+    x = x_dev(synth.gen_x(M, K, g, "bf16"))
+    yM = kq.matvec(qtype, W, x, N, K)
+    for m in range(M):
+        assert torch.equal(yM[m], kq.matvec(qtype, W, x[m:m + 1], N, K)[0]), m
 
 
 @pytest.mark.parametrize("qtype", TYPES)
 @pytest.mark.parametrize("NK", [(1, 256), (129, 704), (300, 2816), (128, 4096 + 96), (2600, 9728)])
-def test_matvec_two_tokens_ragged(qtype, NK):
-    """M = 2 with bf16 x runs the one-token kernel with two x images: ragged
+@pytest.mark.parametrize("M", [2, 3, 4])
+def test_matvec_few_tokens_ragged(qtype, NK, M):
+    """M = 2..4 with bf16 x runs the one-token kernel with M x images: ragged
     tiles, K tails, and tile heights of 32, 16 and 8 rows."""
     N, K = NK
-    y, yr, sr = _matvec_case(qtype, N, K, 2, "bf16", 211)
+    y, yr, sr = _matvec_case(qtype, N, K, M, "bf16", 211)
     assert rel_err(y, yr, sr) <= TOL["bf16"]
 
 
