@@ -319,13 +319,13 @@ def run_workload(args):
         line("single Q4_K 4096x4096, fp32 x, M=1", b, ms, {})
     elif wl == "format_sweep":
         res = {}
-        for qt, nm in ((synth.Q4_K, "Q4_K"), (synth.Q5_K, "Q5_K"), (synth.Q6_K, "Q6_K")):
+        for qt, nm in ((synth.Q4_K, "Q4_K"), (synth.Q5_K, "Q5_K"), (synth.Q6_K, "Q6_K"), (synth.IA4, "IA4")):
             for M in (1, 2, 4, 8):
                 b, ms = dense(qt, 4096, 14336, M, "bf16", 1, nm)
                 res[f"{nm}/M={M}"] = {"ms": ms, "GB/s": b / (ms * 1e-3) / 1e9, "bytes": b}
         tot_b = sum(r["bytes"] for r in res.values())
         tot_ms = sum(r["ms"] for r in res.values())
-        line("format sweep 4096x14336, Q4_K/Q5_K/Q6_K, M=1,2,4,8, bf16 x", tot_b, tot_ms, {"cases": res})
+        line("format sweep 4096x14336, Q4_K/Q5_K/Q6_K/IA4, M=1,2,4,8, bf16 x", tot_b, tot_ms, {"cases": res})
     elif wl == "verify16":
         res, tot_b, tot_ms = {}, 0, 0.0
         for nm, N, K in (("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)):
@@ -358,22 +358,32 @@ def run_workload(args):
              {"cases": res})
     elif wl == "moe":
         E, H, F, SH, top_k, layers = 128, 2816, 704, 2112, 8, 30
-        for M, rho in ((1, 0.0), (8, 0.62), (16, 0.0)):  # M = 8: a verify block's correlated routing
+
+        def mat(qt, N, K, g):
+            # IA4: drawn in MLX's group-affine layout and regrouped on the device (load time, untimed)
+            if qt == synth.IA4:
+                q, sc, bi = synth.gen_ia4_mlx(N, K, g)
+                return kq.ia4_pack(torch.from_numpy(q.view(np.int32)).to(dev),
+                                   torch.from_numpy(sc.view(np.int16)).to(dev),
+                                   torch.from_numpy(bi.view(np.int16)).to(dev))
+            return torch.from_numpy(synth.gen_matrix(qt, N, K, g)).to(dev)
+
+        # M = 8: a verify block's correlated routing; IA4: the group-affine INT4 experts of an MLX checkpoint
+        for M, rho, qt in ((1, 0.0, synth.Q4_K), (1, 0.0, synth.IA4), (8, 0.62, synth.Q4_K), (8, 0.62, synth.IA4),
+                           (16, 0.0, synth.Q4_K)):
             g = synth.rng(2, M)
-            Wg0 = synth.gen_matrix(synth.Q4_K, E * F, H, g)
-            Wd0 = synth.gen_matrix(synth.Q4_K, E * H, F, g)
+            Wg0 = mat(qt, E * F, H, g)
+            Wd0 = mat(qt, E * H, F, g)
             per_layer = []
             for li in range(layers):
                 gl = synth.rng(2, M, li)
-                lay = {"Wg": torch.from_numpy(Wg0).to(dev), "Wu": torch.from_numpy(Wg0).to(dev),
-                       "Wd": torch.from_numpy(Wd0).to(dev),
+                lay = {"Wg": Wg0.clone(), "Wu": Wg0.clone(), "Wd": Wd0.clone(),
                        "logits": torch.from_numpy(synth.gen_logits(M, E, gl, rho=rho)).to(dev),
                        "ids": torch.empty((M, top_k), dtype=torch.int32, device=dev),
                        "gate": torch.empty((M, top_k), dtype=torch.float32, device=dev),
-                       "Sg": torch.from_numpy(synth.gen_matrix(synth.Q4_K, SH, H, gl)).to(dev),
-                       "Su": torch.from_numpy(synth.gen_matrix(synth.Q4_K, SH, H, gl)).to(dev),
-                       "Sd": torch.from_numpy(synth.gen_matrix(synth.Q4_K, H, SH, gl)).to(dev)}
+                       "Sg": mat(qt, SH, H, gl), "Su": mat(qt, SH, H, gl), "Sd": mat(qt, H, SH, gl)}
                 per_layer.append(lay)
+            del Wg0, Wd0
             x = bf16(synth.gen_x(M, H, g, "bf16"))
             xs = bf16(synth.gen_x(M * top_k, F, g, "bf16"))
             xsh = bf16(synth.gen_x(M, SH, g, "bf16"))
@@ -385,11 +395,12 @@ def run_workload(args):
             ysd = torch.empty((M, H), dtype=torch.float32, device=dev)
             wsg = kq.moe_workspace(F, M, top_k, E)
             wsd = kq.moe_workspace(H, M, top_k, E)
-            if M == 1:  # one token: the shared gate|up (same x) as one barrier-free chain launch
+            use_chain = M == 1 and qt != synth.IA4  # chains take the k-quants only
+            if use_chain:  # one token: the shared gate|up (same x) as one barrier-free chain launch
                 for L in per_layer:
                     L["shared_gu"] = kq.Chain([
-                        {"type": synth.Q4_K, "x_dtype": kq.KQ_BF16, "W": L["Sg"], "x": x, "y": ysg, "N": SH, "K": H},
-                        {"type": synth.Q4_K, "x_dtype": kq.KQ_BF16, "W": L["Su"], "x": x, "y": ysu, "N": SH, "K": H}])
+                        {"type": qt, "x_dtype": kq.KQ_BF16, "W": L["Sg"], "x": x, "y": ysg, "N": SH, "K": H},
+                        {"type": qt, "x_dtype": kq.KQ_BF16, "W": L["Su"], "x": x, "y": ysu, "N": SH, "K": H}])
 
             def route_all():
                 for L in per_layer:
@@ -398,23 +409,23 @@ def run_workload(args):
             def step():
                 for L in per_layer:
                     kq.kq_moe_route(L["logits"], M, E, top_k, L["ids"], L["gate"], None, stream)
-                    kq.kq_moe_matvec(synth.Q4_K, L["Wg"], E, L["ids"], None, x, kq.KQ_BF16, 0, yg, F, H, M, top_k,
+                    kq.kq_moe_matvec(qt, L["Wg"], E, L["ids"], None, x, kq.KQ_BF16, 0, yg, F, H, M, top_k,
                                      wsg, wsg.numel(), stream)
-                    kq.kq_moe_matvec(synth.Q4_K, L["Wu"], E, L["ids"], None, x, kq.KQ_BF16, 0, yu, F, H, M, top_k,
+                    kq.kq_moe_matvec(qt, L["Wu"], E, L["ids"], None, x, kq.KQ_BF16, 0, yu, F, H, M, top_k,
                                      wsg, wsg.numel(), stream)
-                    kq.kq_moe_matvec(synth.Q4_K, L["Wd"], E, L["ids"], L["gate"], xs, kq.KQ_BF16, 1, yd, H, F, M,
+                    kq.kq_moe_matvec(qt, L["Wd"], E, L["ids"], L["gate"], xs, kq.KQ_BF16, 1, yd, H, F, M,
                                      top_k, wsd, wsd.numel(), stream)
-                    if M == 1:
+                    if use_chain:
                         L["shared_gu"].run(stream)
                     else:
-                        kq.kq_matvec(synth.Q4_K, L["Sg"], x, kq.KQ_BF16, ysg, SH, H, M, stream)
-                        kq.kq_matvec(synth.Q4_K, L["Su"], x, kq.KQ_BF16, ysu, SH, H, M, stream)
-                    kq.kq_matvec(synth.Q4_K, L["Sd"], xsh, kq.KQ_BF16, ysd, H, SH, M, stream)
+                        kq.kq_matvec(qt, L["Sg"], x, kq.KQ_BF16, ysg, SH, H, M, stream)
+                        kq.kq_matvec(qt, L["Su"], x, kq.KQ_BF16, ysu, SH, H, M, stream)
+                    kq.kq_matvec(qt, L["Sd"], xsh, kq.KQ_BF16, ysd, H, SH, M, stream)
             # the layer as one expert FFN: router, gate|up + activation, down + combine + shared (3 launches)
             wsf = kq.moe_ffn_workspace(H, F, SH, M, top_k, E)
             yf = torch.empty((M, H), dtype=torch.float32, device=dev)
             for L in per_layer:
-                L["ffn"] = kq.ffn_weights(synth.Q4_K, synth.Q4_K, E, kq.KQ_ACT_GELU_TANH, F, L["Wg"], L["Wu"],
+                L["ffn"] = kq.ffn_weights(qt, qt, E, kq.KQ_ACT_GELU_TANH, F, L["Wg"], L["Wu"],
                                           L["Wd"], SH, L["Sg"], L["Su"], L["Sd"])
 
             def step_ffn():
@@ -430,12 +441,16 @@ def run_workload(args):
             route_ms = _timed_graph(torch, route_all, stream, args.steps, args.warmup)
             for L in per_layer:  # distinct experts the router picked (the expert bytes a step reads)
                 L["nexp"] = int(torch.unique(L["ids"]).numel())
-            eb = synth.matrix_bytes(synth.Q4_K, F, H) * 2 + synth.matrix_bytes(synth.Q4_K, H, F)
-            sb = synth.matrix_bytes(synth.Q4_K, SH, H) * 2 + synth.matrix_bytes(synth.Q4_K, H, SH)
+            eb = synth.matrix_bytes(qt, F, H) * 2 + synth.matrix_bytes(qt, H, F)
+            sb = synth.matrix_bytes(qt, SH, H) * 2 + synth.matrix_bytes(qt, H, SH)
             nbytes = sum(L["nexp"] * eb + sb for L in per_layer)
+            # the same without the padding of the last block of rows whose K is not a multiple of 256
+            ub = lambda N, K: N * K * synth.BLOCK_BYTES[qt] // 256  # noqa: E731
+            nbytes_unpadded = sum(L["nexp"] * (2 * ub(F, H) + ub(H, F)) + 2 * ub(SH, H) + ub(H, SH) for L in per_layer)
             line(f"routed MoE decode, 30 layers: router + expert FFN (128 experts top-8, GELU-gated) + shared FFN, "
-                 f"Q4_K, M={M}" + (f", correlated routing (rho {rho})" if rho else ""), nbytes, ms,
+                 f"{synth.TYPE_NAMES[qt]}, M={M}" + (f", correlated routing (rho {rho})" if rho else ""), nbytes, ms,
                  {"tok_s_equiv": M * 1e3 / ms, "distinct_experts_per_layer": sum(L["nexp"] for L in per_layer) / layers,
+                  "weight_bytes_unpadded_per_step": nbytes_unpadded,
                   "launches_per_step": 3 * layers, "router_us_per_layer": route_ms * 1e3 / layers,
                   "separate_products": {"ms_per_step": ms_sep, "GB/s": nbytes / (ms_sep * 1e-3) / 1e9,
                                         "launches_per_step": (6 if M == 1 else 7) * layers}})

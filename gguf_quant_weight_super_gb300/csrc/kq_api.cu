@@ -51,7 +51,8 @@ static kq_status cuda_status(cudaError_t e) {
   return KQ_ERR_CUDA;
 }
 
-static bool valid_type(int t) { return t == KQ_Q4_K || t == KQ_Q5_K || t == KQ_Q6_K; }
+static bool valid_type(int t) { return t == KQ_Q4_K || t == KQ_Q5_K || t == KQ_Q6_K || t == KQ_IA4; }
+static bool kquant_type(int t) { return t == KQ_Q4_K || t == KQ_Q5_K || t == KQ_Q6_K; }  // unpack, chains
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace kq
@@ -62,9 +63,19 @@ extern "C" {
 
 size_t kq_block_bytes(int type) { return valid_type(type) ? static_cast<size_t>(block_bytes_of(type)) : 0; }
 
+kq_status kq_ia4_pack(const uint32_t* q, const uint16_t* scales, const uint16_t* biases, int64_t N, int64_t K,
+                      void* blocks, kq_stream_t stream) {
+  if (N < 0 || K < 0) return KQ_ERR_ARG;
+  if (K % 64) return KQ_ERR_SHAPE;
+  if (N == 0 || K == 0) return KQ_OK;
+  if (!q || !scales || !biases || !blocks) return KQ_ERR_ARG;
+  if (!aligned(q, 4) || !aligned(scales, 2) || !aligned(biases, 2) || !aligned(blocks, 16)) return KQ_ERR_ALIGN;
+  return cuda_status(launch_ia4_pack(q, scales, biases, N, K, blocks, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kq_status kq_unpack(int type, const void* blocks, int64_t n_blocks, uint8_t* codes, int8_t* scales, uint8_t* mins,
                     uint16_t* d_bits, uint16_t* dmin_bits, kq_stream_t stream) {
-  if (!valid_type(type)) return KQ_ERR_TYPE;
+  if (!kquant_type(type)) return KQ_ERR_TYPE;
   if (n_blocks < 0) return KQ_ERR_ARG;
   if (n_blocks == 0) return KQ_OK;
   if (!blocks) return KQ_ERR_ARG;
@@ -129,7 +140,7 @@ static kq_status check_chain(const kq_op* ops, int n_ops) {
   int last_wait = 0;
   for (int i = 0; i < n_ops; ++i) {
     const kq_op& o = ops[i];
-    if (!valid_type(o.type)) return KQ_ERR_TYPE;
+    if (!kquant_type(o.type)) return KQ_ERR_TYPE;
     if (o.x_dtype != KQ_F32 && o.x_dtype != KQ_BF16) return KQ_ERR_ARG;
     if (o.reserved != 0 || o.N <= 0 || o.K <= 0) return KQ_ERR_ARG;
     if (o.K % 32) return KQ_ERR_SHAPE;

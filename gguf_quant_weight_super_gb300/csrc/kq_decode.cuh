@@ -9,6 +9,14 @@
 //                                                       w = d*sc_j*(q - 32)
 // ("GGUF in transformers", section "What is the GGUF file format?", names the
 // Q4_K_M / Q5_K_M / Q6_K variants these blocks make up.)
+//   IA4,  144 B: 4 bf16 scales | 4 bf16 biases | 128 B of 4-bit codes in the
+//                Q4_K code order; group g = weights 64g..64g+63 (sub-blocks
+//                2g, 2g+1).                      w = scale_g*q + bias_g
+//                The group-affine INT4 format of an MLX 4-bit checkpoint
+//                ("ANE Fieldfare" README, "Requirements": the model is an
+//                mlx-community 4-bit checkpoint), regrouped by kq_ia4_pack into
+//                blocks of 256 weights.  It decodes as Q4_K with, per group,
+//                d*sc := scale_g and dmin*m := -bias_g (sc = m = 1).
 //
 // Work split: a block is decoded by 8 lanes; lane j owns 32 of its weights,
 // as P "parts" of L consecutive weights:
@@ -31,15 +39,19 @@
 
 namespace kq {
 
-enum : int { T_Q4_K = 1, T_Q5_K = 2, T_Q6_K = 3 };
+enum : int { T_Q4_K = 1, T_Q5_K = 2, T_Q6_K = 3, T_IA4 = 4 };
+
+// Q4_K and IA4 share the code layout (nibbles of 128 bytes after a 16-byte header).
+template <int QT> constexpr bool kQ4Codes = (QT == T_Q4_K || QT == T_IA4);
 
 template <int QT> struct Fmt;
 template <> struct Fmt<T_Q4_K> { static constexpr int BYTES = 144, P = 2, L = 16, SHIFT = 4; };
 template <> struct Fmt<T_Q5_K> { static constexpr int BYTES = 176, P = 2, L = 16, SHIFT = 5; };
 template <> struct Fmt<T_Q6_K> { static constexpr int BYTES = 210, P = 4, L = 8, SHIFT = 6; };
+template <> struct Fmt<T_IA4> { static constexpr int BYTES = 144, P = 2, L = 16, SHIFT = 4; };
 
 __host__ __device__ constexpr int block_bytes_of(int qt) {
-  return qt == T_Q4_K ? 144 : qt == T_Q5_K ? 176 : qt == T_Q6_K ? 210 : 0;
+  return (qt == T_Q4_K || qt == T_IA4) ? 144 : qt == T_Q5_K ? 176 : qt == T_Q6_K ? 210 : 0;
 }
 
 // Position (within the block) of the first weight of part p of lane j.
@@ -51,6 +63,17 @@ __device__ __forceinline__ int part_pos(int j, int p) {
 
 __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// IA4 group g of a block header (words x, y: scales 0-1, 2-3; z, w: biases):
+// d := scale_g, dmin := -bias_g, so that the Q4_K formulas apply with sc = m = 1.
+__device__ __forceinline__ float ia4_scale(uint4 hdr, int g) {
+  return bf16_bits_to_float(((g < 2 ? hdr.x : hdr.y) >> (16 * (g & 1))) & 0xFFFFu);
+}
+__device__ __forceinline__ float ia4_neg_bias(uint4 hdr, int g) {
+  return -bf16_bits_to_float(((g < 2 ? hdr.z : hdr.w) >> (16 * (g & 1))) & 0xFFFFu);
 }
 
 // f = 1 + q / 2^s from a byte holding 0x80 | (q << (7 - s)): the byte becomes
@@ -131,6 +154,7 @@ template <int QT> struct LaneFields {
   int sc[Fmt<QT>::P];     // scale of each part
   int m[Fmt<QT>::P];      // min of each part (Q4_K/Q5_K)
   uint32_t d_bits, dmin_bits;
+  float d, dmin;          // decoded (IA4: scale and minus bias of the lane's group)
 };
 
 template <int QT>
@@ -155,13 +179,15 @@ __device__ __forceinline__ void lane_fields(const uint8_t* blk, int j, LaneField
     o.m[0] = o.m[1] = o.m[2] = o.m[3] = 0;
     o.d_bits = reinterpret_cast<const uint16_t*>(blk + 208)[0];
     o.dmin_bits = 0;
+    o.d = half_bits_to_float(o.d_bits);
+    o.dmin = 0.0f;
   } else {
     const int g = j >> 1, hh = j & 1;
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
-    constexpr int QS = (QT == T_Q4_K) ? 16 : 48;
+    constexpr int QS = kQ4Codes<QT> ? 16 : 48;
     const uint4 qs = *reinterpret_cast<const uint4*>(blk + QS + 32 * g + 16 * hh);
     const uint32_t wq[4] = {qs.x, qs.y, qs.z, qs.w};
-    if constexpr (QT == T_Q4_K) {
+    if constexpr (kQ4Codes<QT>) {
 #pragma unroll
       for (int w = 0; w < 4; ++w) q4k_pre(wq[w], o.pre[w], o.pre[4 + w]);
     } else {
@@ -170,13 +196,22 @@ __device__ __forceinline__ void lane_fields(const uint8_t* blk, int j, LaneField
 #pragma unroll
       for (int w = 0; w < 4; ++w) q5k_pre(wq[w], wh[w], g, o.pre[w], o.pre[4 + w]);
     }
-    const uint32_t v = scale_min_bytes(hdr.y, hdr.z, hdr.w, g);
-    o.sc[0] = v & 0xFF;
-    o.sc[1] = (v >> 8) & 0xFF;
-    o.m[0] = (v >> 16) & 0xFF;
-    o.m[1] = v >> 24;
-    o.d_bits = hdr.x & 0xFFFF;
-    o.dmin_bits = hdr.x >> 16;
+    if constexpr (QT == T_IA4) {
+      o.sc[0] = o.sc[1] = o.m[0] = o.m[1] = 1;
+      o.d_bits = o.dmin_bits = 0;
+      o.d = ia4_scale(hdr, g);
+      o.dmin = ia4_neg_bias(hdr, g);
+    } else {
+      const uint32_t v = scale_min_bytes(hdr.y, hdr.z, hdr.w, g);
+      o.sc[0] = v & 0xFF;
+      o.sc[1] = (v >> 8) & 0xFF;
+      o.m[0] = (v >> 16) & 0xFF;
+      o.m[1] = v >> 24;
+      o.d_bits = hdr.x & 0xFFFF;
+      o.dmin_bits = hdr.x >> 16;
+      o.d = half_bits_to_float(o.d_bits);
+      o.dmin = half_bits_to_float(o.dmin_bits);
+    }
   }
 }
 
@@ -199,7 +234,7 @@ __device__ __forceinline__ void lane_decode(const uint8_t* blk, int j, int nvali
     for (int k = 0; k < 4; ++k) o.f[4 * w + k] = byte_to_f(fl.pre[w], k);
   }
   constexpr float S = static_cast<float>(1 << Fmt<QT>::SHIFT);
-  const float d = half_bits_to_float(fl.d_bits);
+  const float d = fl.d;
   if constexpr (QT == T_Q6_K) {
     const float dS = d * S, dB = -(S + 32.0f) * d;
 #pragma unroll
@@ -210,7 +245,7 @@ __device__ __forceinline__ void lane_decode(const uint8_t* blk, int j, int nvali
       o.B[p] = ok ? dB * sc : 0.0f;
     }
   } else {
-    const float dmin = half_bits_to_float(fl.dmin_bits);
+    const float dmin = fl.dmin;
     const float dS = d * S;
 #pragma unroll
     for (int p = 0; p < 2; ++p) {

@@ -38,8 +38,7 @@ __global__ void __launch_bounds__(THREADS) dequant_kernel(const uint8_t* __restr
        b += static_cast<int64_t>(gridDim.x) * GROUPS) {
     LaneFields<QT> fl;
     lane_fields<QT>(blocks + b * BB, j, fl);
-    const float d = half_bits_to_float(fl.d_bits);
-    const float dmin = half_bits_to_float(fl.dmin_bits);
+    const float d = fl.d, dmin = fl.dmin;
     OutT* o = out + b * 256;
 #pragma unroll
     for (int p = 0; p < P; ++p) {
@@ -118,8 +117,65 @@ cudaError_t launch_dequant(int qtype, const void* blocks, void* out, int out_bf1
     case T_Q4_K * 2 + 1: dequant_kernel<T_Q4_K, uint16_t><<<grid, THREADS, 0, stream>>>(b, oh, n_blocks); break;
     case T_Q5_K * 2 + 1: dequant_kernel<T_Q5_K, uint16_t><<<grid, THREADS, 0, stream>>>(b, oh, n_blocks); break;
     case T_Q6_K * 2 + 1: dequant_kernel<T_Q6_K, uint16_t><<<grid, THREADS, 0, stream>>>(b, oh, n_blocks); break;
+    case T_IA4 * 2: dequant_kernel<T_IA4, float><<<grid, THREADS, 0, stream>>>(b, of, n_blocks); break;
+    case T_IA4 * 2 + 1: dequant_kernel<T_IA4, uint16_t><<<grid, THREADS, 0, stream>>>(b, oh, n_blocks); break;
     default: return cudaErrorInvalidValue;
   }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Group-affine INT4 (an MLX 4-bit checkpoint) -> IA4 blocks.  The source is
+// row-major: codes q[N][K/8] as 32-bit words, code k of a row in bits
+// 4(k%8)..4(k%8)+3 of word k/8; scales and biases [N][K/64] bf16, group
+// G = weights 64G..64G+63, w = scale*q + bias.  One thread per (row, group):
+// the group's scale and bias go to the block header, its 64 codes to the 32
+// code bytes of chunk g = G%4 in the Q4_K order (byte 32g+l: weight 64g+l in
+// the low nibble, 64g+32+l in the high one).  Groups past K in a row's last
+// block get zero scale, bias and codes.
+// ---------------------------------------------------------------------------
+__global__ void ia4_pack_kernel(const uint32_t* __restrict__ q, const uint16_t* __restrict__ scales,
+                                const uint16_t* __restrict__ biases, int64_t N, int64_t K, uint8_t* __restrict__ blocks) {
+  const int64_t ng = K / 64, nb = (K + 255) / 256;
+  const int64_t total = N * nb * 4;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = t / (nb * 4), r = t - n * nb * 4;
+    const int64_t b = r >> 2;
+    const int g = static_cast<int>(r & 3);
+    const int64_t G = 4 * b + g;
+    uint8_t* blk = blocks + (n * nb + b) * 144;
+    const bool in = G < ng;
+    reinterpret_cast<uint16_t*>(blk)[g] = in ? scales[n * ng + G] : static_cast<uint16_t>(0);
+    reinterpret_cast<uint16_t*>(blk + 8)[g] = in ? biases[n * ng + G] : static_cast<uint16_t>(0);
+    uint32_t out[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = 0u;
+    if (in) {
+      const uint32_t* src = q + n * (K / 8) + G * 8;  // the group's 8 words: weights 64G + 8i + j
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = src[i];
+#pragma unroll
+      for (int l = 0; l < 32; ++l) {
+        const uint32_t lo = (w[l >> 3] >> (4 * (l & 7))) & 15u;             // weight 64G + l
+        const uint32_t hi = (w[4 + (l >> 3)] >> (4 * (l & 7))) & 15u;       // weight 64G + 32 + l
+        out[l >> 2] |= (lo | (hi << 4)) << (8 * (l & 3));
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(blk + 16 + 32 * g);
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+}
+
+cudaError_t launch_ia4_pack(const uint32_t* q, const uint16_t* scales, const uint16_t* biases, int64_t N, int64_t K,
+                            void* blocks, cudaStream_t stream) {
+  const int64_t total = N * ((K + 255) / 256) * 4;
+  if (total == 0) return cudaSuccess;
+  const int64_t want = (total + 255) / 256;
+  const int grid = static_cast<int>(want < 152 * 16 ? want : 152 * 16);
+  ia4_pack_kernel<<<grid, 256, 0, stream>>>(q, scales, biases, N, K, static_cast<uint8_t*>(blocks));
   return cudaGetLastError();
 }
 

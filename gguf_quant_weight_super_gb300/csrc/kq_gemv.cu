@@ -733,6 +733,8 @@ cudaError_t launch_single(int qtype, int NL, int R, ProgArgs& a, const LaunchGeo
     case T_Q5_K * 4 + 3: return launch_single_r<T_Q5_K, 3>(R, a, g, st, pdl);
     case T_Q6_K * 4 + 2: return launch_single_r<T_Q6_K, 2>(R, a, g, st, pdl);
     case T_Q6_K * 4 + 3: return launch_single_r<T_Q6_K, 3>(R, a, g, st, pdl);
+    case T_IA4 * 4 + 2: return launch_single_r<T_IA4, 2>(R, a, g, st, pdl);
+    case T_IA4 * 4 + 3: return launch_single_r<T_IA4, 3>(R, a, g, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -772,6 +774,9 @@ cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, 
       case T_Q4_K * 8 + 4: return launch_single_r<T_Q4_K, 2, 4>(o.R, a, g, stream, pdl);
       case T_Q5_K * 8 + 4: return launch_single_r<T_Q5_K, 2, 4>(o.R, a, g, stream, pdl);
       case T_Q6_K * 8 + 4: return launch_single_r<T_Q6_K, 2, 4>(o.R, a, g, stream, pdl);
+      case T_IA4 * 8 + 2: return launch_single_r<T_IA4, 2, 2>(o.R, a, g, stream, pdl);
+      case T_IA4 * 8 + 3: return launch_single_r<T_IA4, 2, 3>(o.R, a, g, stream, pdl);
+      case T_IA4 * 8 + 4: return launch_single_r<T_IA4, 2, 4>(o.R, a, g, stream, pdl);
       default: return cudaErrorInvalidValue;
     }
   }

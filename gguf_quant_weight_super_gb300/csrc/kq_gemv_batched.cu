@@ -49,6 +49,7 @@ template <int QT> struct QuadFmt;
 template <> struct QuadFmt<T_Q4_K> { static constexpr int P = 2, PL = 32; };
 template <> struct QuadFmt<T_Q5_K> { static constexpr int P = 2, PL = 32; };
 template <> struct QuadFmt<T_Q6_K> { static constexpr int P = 4, PL = 16; };
+template <> struct QuadFmt<T_IA4> { static constexpr int P = 2, PL = 32; };
 
 // position within the block of the first weight of part p of quad lane c
 template <int QT>
@@ -234,19 +235,20 @@ __device__ __forceinline__ void do_block(const uint8_t* const (&blk)[R], const b
       }
     } else {
       const uint4 hdr = *reinterpret_cast<const uint4*>(b);
-      constexpr int QS = (QT == T_Q4_K) ? 16 : 48;
+      constexpr int QS = kQ4Codes<QT> ? 16 : 48;
       raw[i][0] = *reinterpret_cast<const uint4*>(b + QS + 32 * c);
       raw[i][1] = *reinterpret_cast<const uint4*>(b + QS + 32 * c + 16);
       if constexpr (QT == T_Q5_K) {
         raw[i][2] = *reinterpret_cast<const uint4*>(b + 16);
         raw[i][3] = *reinterpret_cast<const uint4*>(b + 32);
       }
-      const uint32_t v = scale_min_bytes(hdr.y, hdr.z, hdr.w, c);
-      const float d = half_bits_to_float(hdr.x & 0xFFFF);
-      const float dmin = half_bits_to_float(hdr.x >> 16);
+      // IA4: quad lane c's two parts are group c (sc = m = 1, d = scale, dmin = -bias)
+      const uint32_t v = (QT == T_IA4) ? 0x01010101u : scale_min_bytes(hdr.y, hdr.z, hdr.w, c);
+      const float d = (QT == T_IA4) ? ia4_scale(hdr, c) : half_bits_to_float(hdr.x & 0xFFFF);
+      const float dmin = (QT == T_IA4) ? ia4_neg_bias(hdr, c) : half_bits_to_float(hdr.x >> 16);
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
-        const float sS = (QT == T_Q4_K && p == 1) ? 16.0f : 128.0f;
+        const float sS = (kQ4Codes<QT> && p == 1) ? 16.0f : 128.0f;
         const float av = (sS * d) * static_cast<float>((v >> (8 * p)) & 0xFF);
         const float mm = dmin * static_cast<float>((v >> (16 + 8 * p)) & 0xFF);
         const bool ok = qpos<QT>(c, p) + PL <= rem;
@@ -291,7 +293,7 @@ __device__ __forceinline__ void do_block(const uint8_t* const (&blk)[R], const b
         for (int i = 0; i < R; ++i) {
           if (!rok[i]) continue;
           const uint32_t q = word_of(raw[i][w >> 2], w & 3);
-          if constexpr (QT == T_Q4_K) {
+          if constexpr (kQ4Codes<QT>) {
             Sx[i][0] = fma4(q4_lo(q), xlo, Sx[i][0]);
             Sx[i][1] = fma4(q4_hi(q), xhi, Sx[i][1]);
           } else {
@@ -624,6 +626,7 @@ cudaError_t launch_gemv_batched(int qtype, const void* W, const void* x, int x_b
       case T_Q4_K: e = launch_q<T_Q4_K>(a, p.R, smem, p.grid, stream, pdl); break;
       case T_Q5_K: e = launch_q<T_Q5_K>(a, p.R, smem, p.grid, stream, pdl); break;
       case T_Q6_K: e = launch_q<T_Q6_K>(a, p.R, smem, p.grid, stream, pdl); break;
+      case T_IA4: e = launch_q<T_IA4>(a, p.R, smem, p.grid, stream, pdl); break;
       default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;

@@ -106,6 +106,8 @@ cudaError_t launch_route(const float* logits, int M, int E, int top_k, int* ids,
 
 cudaError_t launch_dequant(int qtype, const void* blocks, void* out, int out_bf16, int64_t n_blocks,
                            cudaStream_t stream);
+cudaError_t launch_ia4_pack(const uint32_t* q, const uint16_t* scales, const uint16_t* biases, int64_t N, int64_t K,
+                            void* blocks, cudaStream_t stream);
 cudaError_t launch_unpack(int qtype, const void* blocks, int64_t n_blocks, uint8_t* codes, int8_t* scales,
                           uint8_t* mins, uint16_t* d_bits, uint16_t* dmin_bits, cudaStream_t stream);
 

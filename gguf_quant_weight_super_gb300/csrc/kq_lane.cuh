@@ -273,7 +273,7 @@ template <int QT, int NL>
 __device__ __forceinline__ float core_q45(uint32_t bp, const XSlice<NL>& X, int2 si, float s, int c,
                                           const ScaleLane& sl, float acc) {
   const uint4 hdr = lds128(bp);
-  constexpr int QS = (QT == T_Q4_K) ? 16 : 48;
+  constexpr int QS = kQ4Codes<QT> ? 16 : 48;
   const uint4 q0 = lds128(bp + QS + 32 * c);
   const uint4 q1 = lds128(bp + QS + 32 * c + 16);
   uint4 h0 = make_uint4(0, 0, 0, 0), h1 = make_uint4(0, 0, 0, 0);
@@ -287,7 +287,7 @@ __device__ __forceinline__ float core_q45(uint32_t bp, const XSlice<NL>& X, int2
   for (int w = 0; w < 8; ++w) {
     const uint32_t q = (w < 4) ? w4(q0, w) : w4(q1, w - 4);
     uint32_t lo, hi;
-    if constexpr (QT == T_Q4_K) {
+    if constexpr (kQ4Codes<QT>) {
       lo = q & 0x0F0F0F0Fu;
       hi = q & 0xF0F0F0F0u;  // 16 x the high nibble: the factor leaves T_1 exactly
     } else {
@@ -304,17 +304,26 @@ __device__ __forceinline__ float core_q45(uint32_t bp, const XSlice<NL>& X, int2
     }
   }
   // scales and mins of sub-blocks 2c, 2c+1
-  const uint32_t P = __byte_perm(sl.lowsrc ? hdr.y : hdr.w, hdr.z, sl.selP);
-  const uint32_t Q = __byte_perm(hdr.y, hdr.z, sl.selQ);
-  const uint32_t L = (P & sl.mA) | ((P >> 4) & sl.mB) | ((Q >> 2) & sl.mH);
-  const int sc0 = static_cast<int>(L & 0xFF), sc1 = static_cast<int>((L >> 8) & 0xFF);
-  const int m0 = static_cast<int>((L >> 16) & 0xFF), m1 = static_cast<int>(L >> 24);
-  const float d = half_bits_to_float(hdr.x & 0xFFFF);
-  const float dmin = half_bits_to_float(hdr.x >> 16);
+  int sc0 = 1, sc1 = 1, m0 = 1, m1 = 1;
+  float d, dmin;
+  if constexpr (QT == T_IA4) {  // the lane's two sub-blocks are group c: one scale, one bias
+    d = ia4_scale(hdr, c);
+    dmin = ia4_neg_bias(hdr, c);
+  } else {
+    const uint32_t P = __byte_perm(sl.lowsrc ? hdr.y : hdr.w, hdr.z, sl.selP);
+    const uint32_t Q = __byte_perm(hdr.y, hdr.z, sl.selQ);
+    const uint32_t L = (P & sl.mA) | ((P >> 4) & sl.mB) | ((Q >> 2) & sl.mH);
+    sc0 = static_cast<int>(L & 0xFF);
+    sc1 = static_cast<int>((L >> 8) & 0xFF);
+    m0 = static_cast<int>((L >> 16) & 0xFF);
+    m1 = static_cast<int>(L >> 24);
+    d = half_bits_to_float(hdr.x & 0xFFFF);
+    dmin = half_bits_to_float(hdr.x >> 16);
+  }
   if constexpr (NL == 2) {
     const int T0 = I[0][0] * 256 + I[0][1];
     int T1 = I[1][0] * 256 + I[1][1];
-    if constexpr (QT == T_Q4_K) T1 >>= 4;  // exact: every term is a multiple of 16
+    if constexpr (kQ4Codes<QT>) T1 >>= 4;  // exact: every term is a multiple of 16
     const int Y = sc0 * T0 + sc1 * T1;
     const int Mi = m0 * si.x + m1 * si.y;
     return __fmaf_rn(s, __fmaf_rn(d, static_cast<float>(Y), -dmin * static_cast<float>(Mi)), acc);
@@ -323,7 +332,7 @@ __device__ __forceinline__ float core_q45(uint32_t bp, const XSlice<NL>& X, int2
 #pragma unroll
     for (int l = 0; l < NL; ++l) {
       int t1 = I[1][l];
-      if constexpr (QT == T_Q4_K) t1 >>= 4;
+      if constexpr (kQ4Codes<QT>) t1 >>= 4;
       Yl[l] = sc0 * I[0][l] + sc1 * t1;
     }
     const float Yf = __fmaf_rn(static_cast<float>(Yl[0]), 65536.0f,
@@ -401,7 +410,7 @@ template <int QT, int NL, int MT>
 __device__ __forceinline__ void core_q45_mt(uint32_t bp, const XSlice<NL> (&X)[MT], const int2 (&si)[MT],
                                             const float (&s)[MT], int c, const ScaleLane& sl, float (&acc)[MT]) {
   const uint4 hdr = lds128(bp);
-  constexpr int QS = (QT == T_Q4_K) ? 16 : 48;
+  constexpr int QS = kQ4Codes<QT> ? 16 : 48;
   const uint4 q0 = lds128(bp + QS + 32 * c);
   const uint4 q1 = lds128(bp + QS + 32 * c + 16);
   uint4 h0 = make_uint4(0, 0, 0, 0), h1 = make_uint4(0, 0, 0, 0);
@@ -417,7 +426,7 @@ __device__ __forceinline__ void core_q45_mt(uint32_t bp, const XSlice<NL> (&X)[M
   for (int w = 0; w < 8; ++w) {
     const uint32_t q = (w < 4) ? w4(q0, w) : w4(q1, w - 4);
     uint32_t lo, hi;
-    if constexpr (QT == T_Q4_K) {
+    if constexpr (kQ4Codes<QT>) {
       lo = q & 0x0F0F0F0Fu;
       hi = q & 0xF0F0F0F0u;  // 16 x the high nibble: the factor leaves T_1 exactly
     } else {
@@ -436,19 +445,28 @@ __device__ __forceinline__ void core_q45_mt(uint32_t bp, const XSlice<NL> (&X)[M
       }
     }
   }
-  const uint32_t P = __byte_perm(sl.lowsrc ? hdr.y : hdr.w, hdr.z, sl.selP);
-  const uint32_t Q = __byte_perm(hdr.y, hdr.z, sl.selQ);
-  const uint32_t L = (P & sl.mA) | ((P >> 4) & sl.mB) | ((Q >> 2) & sl.mH);
-  const int sc0 = static_cast<int>(L & 0xFF), sc1 = static_cast<int>((L >> 8) & 0xFF);
-  const int m0 = static_cast<int>((L >> 16) & 0xFF), m1 = static_cast<int>(L >> 24);
-  const float d = half_bits_to_float(hdr.x & 0xFFFF);
-  const float dmin = half_bits_to_float(hdr.x >> 16);
+  int sc0 = 1, sc1 = 1, m0 = 1, m1 = 1;
+  float d, dmin;
+  if constexpr (QT == T_IA4) {  // the lane's two sub-blocks are group c: one scale, one bias
+    d = ia4_scale(hdr, c);
+    dmin = ia4_neg_bias(hdr, c);
+  } else {
+    const uint32_t P = __byte_perm(sl.lowsrc ? hdr.y : hdr.w, hdr.z, sl.selP);
+    const uint32_t Q = __byte_perm(hdr.y, hdr.z, sl.selQ);
+    const uint32_t L = (P & sl.mA) | ((P >> 4) & sl.mB) | ((Q >> 2) & sl.mH);
+    sc0 = static_cast<int>(L & 0xFF);
+    sc1 = static_cast<int>((L >> 8) & 0xFF);
+    m0 = static_cast<int>((L >> 16) & 0xFF);
+    m1 = static_cast<int>(L >> 24);
+    d = half_bits_to_float(hdr.x & 0xFFFF);
+    dmin = half_bits_to_float(hdr.x >> 16);
+  }
 #pragma unroll
   for (int t = 0; t < MT; ++t) {
     if constexpr (NL == 2) {
       const int T0 = I[t][0][0] * 256 + I[t][0][1];
       int T1 = I[t][1][0] * 256 + I[t][1][1];
-      if constexpr (QT == T_Q4_K) T1 >>= 4;
+      if constexpr (kQ4Codes<QT>) T1 >>= 4;
       const int Y = sc0 * T0 + sc1 * T1;
       const int Mi = m0 * si[t].x + m1 * si[t].y;
       acc[t] = __fmaf_rn(s[t], __fmaf_rn(d, static_cast<float>(Y), -dmin * static_cast<float>(Mi)), acc[t]);
@@ -457,7 +475,7 @@ __device__ __forceinline__ void core_q45_mt(uint32_t bp, const XSlice<NL> (&X)[M
 #pragma unroll
       for (int l = 0; l < NL; ++l) {
         int t1 = I[t][1][l];
-        if constexpr (QT == T_Q4_K) t1 >>= 4;
+        if constexpr (kQ4Codes<QT>) t1 >>= 4;
         Yl[l] = sc0 * I[t][0][l] + sc1 * t1;
       }
       const float Yf = __fmaf_rn(static_cast<float>(Yl[0]), 65536.0f,

@@ -458,6 +458,8 @@ cudaError_t launch_args(MoeArgs& a, int qtype, cudaStream_t st) {
     case T_Q5_K * 4 + 3: return launch_moe_t<T_Q5_K, 3>(a, smem, st);
     case T_Q6_K * 4 + 2: return launch_moe_t<T_Q6_K, 2>(a, smem, st);
     case T_Q6_K * 4 + 3: return launch_moe_t<T_Q6_K, 3>(a, smem, st);
+    case T_IA4 * 4 + 2: return launch_moe_t<T_IA4, 2>(a, smem, st);
+    case T_IA4 * 4 + 3: return launch_moe_t<T_IA4, 3>(a, smem, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -110,7 +110,7 @@ __device__ __forceinline__ void four_weights(uint32_t v, int pos, float A, float
 template <int QT>
 __device__ __forceinline__ void dequant_half(uint32_t bp, int g, uint32_t taddr) {
   uint32_t col[16];
-  if constexpr (QT == T_Q4_K || QT == T_Q5_K) {
+  if constexpr (QT != T_Q6_K) {
     const uint4 hdr = lds128(bp);
     const float d = half_bits_to_float(hdr.x & 0xFFFF), dmin = half_bits_to_float(hdr.x >> 16);
     // scales and mins of sub-blocks 4g .. 4g+3 (bytes)
@@ -122,23 +122,29 @@ __device__ __forceinline__ void dequant_half(uint32_t bp, int g, uint32_t taddr)
       scb = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
       mb = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
     }
-    constexpr int QS = (QT == T_Q4_K) ? 16 : 48;
+    constexpr int QS = kQ4Codes<QT> ? 16 : 48;
     uint4 qh0 = make_uint4(0, 0, 0, 0), qh1 = qh0;
     if constexpr (QT == T_Q5_K) { qh0 = lds128(bp + 16); qh1 = lds128(bp + 32); }
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {  // chunk c = 2g + cc: sub-blocks 2c (low nibbles), 2c+1 (high)
       const int c = 2 * g + cc;
-      const float dsl = d * static_cast<float>((scb >> (16 * cc)) & 0xFF);
-      const float dml = dmin * static_cast<float>((mb >> (16 * cc)) & 0xFF);
-      const float dsh = d * static_cast<float>((scb >> (16 * cc + 8)) & 0xFF);
-      const float dmh = dmin * static_cast<float>((mb >> (16 * cc + 8)) & 0xFF);
+      float dsl, dml, dsh, dmh;
+      if constexpr (QT == T_IA4) {  // chunk c is group c: one scale and one bias for both sub-blocks
+        dsl = dsh = ia4_scale(hdr, c);
+        dml = dmh = ia4_neg_bias(hdr, c);
+      } else {
+        dsl = d * static_cast<float>((scb >> (16 * cc)) & 0xFF);
+        dml = dmin * static_cast<float>((mb >> (16 * cc)) & 0xFF);
+        dsh = d * static_cast<float>((scb >> (16 * cc + 8)) & 0xFF);
+        dmh = dmin * static_cast<float>((mb >> (16 * cc + 8)) & 0xFF);
+      }
       const uint4 qa = lds128(bp + QS + 32 * c), qb = lds128(bp + QS + 32 * c + 16);
 #pragma unroll
       for (int part = 0; part < 2; ++part) {  // 0: low nibbles, 1: high nibbles
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
           const uint32_t q = (w < 4) ? w4(qa, w) : w4(qb, w - 4);
-          if constexpr (QT == T_Q4_K) {
+          if constexpr (kQ4Codes<QT>) {
             if (part == 0) {
               // 0.5 + q/256, q in 0..15:  w = f*(256 d sc) - (128 d sc + dmin m)
               four_weights(q & 0x0F0F0F0Fu, 2, 256.0f * dsl, -(128.0f * dsl + dml), col[2 * w], col[2 * w + 1]);
@@ -530,9 +536,10 @@ cudaError_t launch_tc(int qtype, const void* W, const void* x, float* y, int64_t
     case T_Q4_K: fn = reinterpret_cast<const void*>(tc_kernel<T_Q4_K>); break;
     case T_Q5_K: fn = reinterpret_cast<const void*>(tc_kernel<T_Q5_K>); break;
     case T_Q6_K: fn = reinterpret_cast<const void*>(tc_kernel<T_Q6_K>); break;
+    case T_IA4: fn = reinterpret_cast<const void*>(tc_kernel<T_IA4>); break;
     default: return cudaErrorInvalidValue;
   }
-  static bool smem_set[64][4] = {};
+  static bool smem_set[64][8] = {};
   const int dev = current_device_id();
   if (!smem_set[dev][qtype]) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemPerBlock);

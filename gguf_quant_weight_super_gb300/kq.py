@@ -15,7 +15,7 @@ import torch
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libkq.so")
 
-KQ_Q4_K, KQ_Q5_K, KQ_Q6_K = 1, 2, 3
+KQ_Q4_K, KQ_Q5_K, KQ_Q6_K, KQ_IA4 = 1, 2, 3, 4
 KQ_F32, KQ_BF16 = 0, 1
 KQ_ACT_SILU, KQ_ACT_GELU_TANH = 0, 1
 KQ_OK = 0
@@ -26,6 +26,7 @@ STATUS = {0: "KQ_OK", -1: "KQ_ERR_ARG", -2: "KQ_ERR_TYPE", -3: "KQ_ERR_SHAPE", -
 _P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 SIGNATURES = {
     "kq_block_bytes": (_SZ, [_I]),
+    "kq_ia4_pack": (_I, [_P, _P, _P, _I64, _I64, _P, _P]),
     "kq_unpack": (_I, [_I, _P, _I64, _P, _P, _P, _P, _P, _P]),
     "kq_dequant": (_I, [_I, _P, _P, _I64, _P]),
     "kq_dequant_bf16": (_I, [_I, _P, _P, _I64, _P]),
@@ -152,6 +153,20 @@ def moe_route(logits: torch.Tensor, top_k: int, workspace=None, stream=None):
     gate = torch.empty((M, top_k), dtype=torch.float32, device=logits.device)
     kq_moe_route(logits, M, E, top_k, ids, gate, workspace, stream)
     return ids, gate
+
+
+def kq_ia4_pack(q, scales, biases, N, K, blocks, stream=None):
+    _check("kq_ia4_pack", lib().kq_ia4_pack(_ptr(q), _ptr(scales), _ptr(biases), N, K, _ptr(blocks),
+                                            _stream(stream)))
+
+
+def ia4_pack(q: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor) -> torch.Tensor:
+    """MLX group-affine INT4 arrays (int32 codes [N, K/8], bf16-bit scales and
+    biases [N, K/64] as int16 or bfloat16) -> KQ_IA4 blocks (uint8)."""
+    N, K = q.shape[0], q.shape[1] * 8
+    out = torch.empty(N * ((K + 255) // 256) * 144, dtype=torch.uint8, device=q.device)
+    kq_ia4_pack(q, scales, biases, N, K, out)
+    return out
 
 
 def kq_dequant_bf16(qtype, blocks, out, n, stream=None):

@@ -11,10 +11,15 @@ bytes placed at each field's byte offset:
 * Q6_K scales are int8 drawn uniformly from a given range;
 * ``d`` / ``dmin`` are ``|N(0, sigma)|`` rounded to fp16 (round to nearest even).
 
+IA4 (group-affine INT4) blocks put bf16 scales ``|N(0, sigma)|`` and biases
+``-8 * scale * (1 + N(0, 1)/4)`` in the header and uniform random code bytes
+after it; ``gen_ia4_mlx`` draws the same kind of matrix in MLX's layout (code
+words, scales, biases).
+
 Activations are fp32 N(0, 1), optionally rounded to bfloat16 (nearest even) and
-returned as raw bit patterns.  Routing draws N(0, 1) router logits per token,
-keeps the ``top_k`` largest (ties to the lower expert index) and takes a softmax
-over the kept logits as gate weights; routing is an input of the product.
+returned as raw bit patterns.  Routing inputs are drawn directly: distinct
+expert ids uniform per token and flat-Dirichlet gate weights, or router logits
+(N(0, 1), integer-valued, or with a component shared by all tokens).
 
 Used by the tests (feeding the oracle and the CUDA path the same bytes) and by
 the benchmark.
@@ -24,9 +29,9 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-Q4_K, Q5_K, Q6_K = 1, 2, 3
-TYPE_NAMES = {Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K"}
-BLOCK_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210}
+Q4_K, Q5_K, Q6_K, IA4 = 1, 2, 3, 4
+TYPE_NAMES = {Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K", IA4: "IA4"}
+BLOCK_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210, IA4: 144}
 QK = 256
 
 # byte offsets of the fields of one block (format reading; see the design notes)
@@ -57,6 +62,11 @@ def gen_blocks(qtype: int, n_blocks: int, g: np.random.Generator, *, d_sigma: fl
     """``n_blocks`` random blocks as a (n_blocks, block_bytes) uint8 array."""
     nbytes = BLOCK_BYTES[qtype]
     out = g.integers(0, 256, size=(n_blocks, nbytes), dtype=np.uint8)
+    if qtype == IA4:
+        s, b = _ia4_scale_bias(g, n_blocks * 4, d_sigma)
+        out[:, 0:8] = s.reshape(n_blocks, 4).astype("<u2").view(np.uint8).reshape(n_blocks, 8)
+        out[:, 8:16] = b.reshape(n_blocks, 4).astype("<u2").view(np.uint8).reshape(n_blocks, 8)
+        return out
     d = _half_bits(g, n_blocks, d_sigma)
     o = _D_OFF[qtype]
     out[:, o] = (d & 0xFF).astype(np.uint8)
@@ -72,6 +82,26 @@ def gen_blocks(qtype: int, n_blocks: int, g: np.random.Generator, *, d_sigma: fl
         sc = g.integers(lo, hi + 1, size=(n_blocks, cnt), dtype=np.int64).astype(np.int8)
         out[:, off:off + cnt] = sc.view(np.uint8)
     return out
+
+
+def _bf16_bits_of(v: np.ndarray) -> np.ndarray:
+    u = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _ia4_scale_bias(g: np.random.Generator, n: int, sigma: float):
+    """bf16 bit patterns of n scales |N(0, sigma)| and biases -8 * scale * (1 + N(0,1)/4)."""
+    s = np.abs(g.normal(0.0, sigma, n)).astype(np.float32)
+    b = (-8.0 * s * (1.0 + 0.25 * g.standard_normal(n))).astype(np.float32)
+    return _bf16_bits_of(s), _bf16_bits_of(b)
+
+
+def gen_ia4_mlx(N: int, K: int, g: np.random.Generator, sigma: float = 0.002):
+    """A group-affine INT4 matrix in MLX's layout: (code words uint32 [N, K/8],
+    scales bf16 bits [N, K/64], biases bf16 bits [N, K/64]); K a multiple of 64."""
+    q = g.integers(0, 2 ** 32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+    s, b = _ia4_scale_bias(g, N * (K // 64), sigma)
+    return q, s.reshape(N, K // 64), b.reshape(N, K // 64)
 
 
 def gen_matrix(qtype: int, N: int, K: int, g: np.random.Generator, **kw) -> np.ndarray:

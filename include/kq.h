@@ -24,6 +24,14 @@
  *   KQ_Q5_K  176 B: as Q4_K with 32 B of 5th code bits before the codes (q in 0..31).
  *   KQ_Q6_K  210 B: 128 B low nibbles | 64 B high bit pairs | 16 int8 scales | d fp16.
  *            w = d*sc_j*(q - 32), j = 16-weight sub-block, q in 0..63
+ *   KQ_IA4   144 B: 4 bf16 scales | 4 bf16 biases | 128 B 4-bit codes in the
+ *            Q4_K code order (byte 32g+l: weight 64g+l low nibble, 64g+32+l
+ *            high nibble).  w = scale_g*q + bias_g, g = 64-weight group.
+ *            Group-affine INT4 ("ANE Fieldfare" README, "Requirements": the
+ *            experts come from an mlx-community 4-bit checkpoint; the pages do
+ *            not print its layout -- this library takes MLX's affine form,
+ *            groups of 64, bf16 scales and biases), regrouped from MLX's
+ *            arrays by kq_ia4_pack.  Not accepted by kq_unpack or chains.
  *
  * Matrices: W has N rows; row n is ceil(K/256) consecutive blocks, rows are
  * consecutive (no padding).  Weights at positions k >= K in a row's last block
@@ -63,7 +71,7 @@ extern "C" {
 
 typedef struct CUstream_st *kq_stream_t; /* same type as cudaStream_t */
 
-typedef enum { KQ_Q4_K = 1, KQ_Q5_K = 2, KQ_Q6_K = 3 } kq_type;
+typedef enum { KQ_Q4_K = 1, KQ_Q5_K = 2, KQ_Q6_K = 3, KQ_IA4 = 4 } kq_type;
 typedef enum { KQ_F32 = 0, KQ_BF16 = 1 } kq_dtype;
 
 typedef int kq_status;
@@ -77,8 +85,21 @@ typedef int kq_status;
 #define KQ_ERR_WORKSPACE (-7)   /* workspace missing or too small                */
 #define KQ_ERR_DEVICE (-8)      /* the device error word was set (kq_device_error) */
 
-/* Bytes of one 256-weight block: 144, 176, 210; 0 for an unknown type. */
+/* Bytes of one 256-weight block: 144, 176, 210, 144; 0 for an unknown type. */
 size_t kq_block_bytes(int type);
+
+/*
+ * Regroup a group-affine INT4 matrix in MLX's layout into KQ_IA4 blocks.
+ *   q       [N][K/8] uint32: code k of a row in bits 4(k%8)..4(k%8)+3 of word k/8
+ *   scales  [N][K/64] bf16 bit patterns, biases [N][K/64]: group G covers
+ *           weights 64G..64G+63, w = scale*q + bias
+ *   blocks  [N][ceil(K/256)] KQ_IA4 blocks (16-byte aligned); groups past K
+ *           in a row's last block get zero scale, bias and codes.
+ * K a multiple of 64 (else KQ_ERR_SHAPE); q 4-byte, scales and biases 2-byte
+ * aligned.  Stream-ordered, one launch; a load-time conversion, not a product.
+ */
+kq_status kq_ia4_pack(const uint32_t *q, const uint16_t *scales, const uint16_t *biases, int64_t N, int64_t K,
+                      void *blocks, kq_stream_t stream);
 
 /*
  * Integer fields of n_blocks consecutive blocks (the super-block unpacker the

@@ -17,9 +17,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "kq_oracle.c")
 LIB = os.path.join(HERE, "libkq_oracle.so")
 
-Q4_K, Q5_K, Q6_K = 1, 2, 3
+Q4_K, Q5_K, Q6_K, IA4 = 1, 2, 3, 4
 X_F32, X_BF16 = 0, 1
-BLOCK_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210}
+BLOCK_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210, IA4: 144}
 
 
 def build(force: bool = False) -> str:
@@ -321,3 +321,44 @@ def moe_ffn(type_gu: int, W_gate, W_up, type_dn: int, W_down, n_experts: int, id
         out["y"] += hs @ Cd.T
         out["s"] += np.abs(hs) @ np.abs(Cd).T
     return out
+
+
+def _bf16_f64(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def ia4_dequant_mlx(q: np.ndarray, scales: np.ndarray, biases: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Group-affine INT4 by its definition, straight from MLX's arrays (fp64
+    [N, K]): code k of row n = bits 4(k%8).. of word q[n, k//8], w = scale *
+    code + bias with the bf16 scale and bias of group k//64.  "ANE Fieldfare"
+    README, "Requirements": the experts are an mlx-community 4-bit
+    checkpoint; reading: MLX's affine form, groups of 64."""
+    q = np.asarray(q, dtype=np.uint32).reshape(N, K // 8)
+    k = np.arange(K)
+    codes = (q[:, k // 8] >> (4 * (k % 8)).astype(np.uint32)) & 15
+    s = _bf16_f64(np.asarray(scales).reshape(N, K // 64))[:, k // 64]
+    b = _bf16_f64(np.asarray(biases).reshape(N, K // 64))[:, k // 64]
+    return s * codes.astype(np.float64) + b
+
+
+def ia4_pack(q: np.ndarray, scales: np.ndarray, biases: np.ndarray, N: int, K: int) -> np.ndarray:
+    """MLX's arrays -> IA4 blocks (uint8, N * ceil(K/256) * 144 bytes), by the
+    block layout: per block, 4 bf16 scales, 4 bf16 biases, then for group g
+    and l < 32 the byte (code of weight 64g+l) | (code of weight 64g+32+l) << 4;
+    groups past K are zero."""
+    q = np.asarray(q, dtype=np.uint32).reshape(N, K // 8)
+    scales = np.asarray(scales, dtype=np.uint16).reshape(N, K // 64)
+    biases = np.asarray(biases, dtype=np.uint16).reshape(N, K // 64)
+    nb = (K + 255) // 256
+    out = np.zeros((N, nb, 144), dtype=np.uint8)
+    for n in range(N):
+        for G in range(K // 64):
+            b, g = divmod(G, 4)
+            out[n, b, 2 * g:2 * g + 2] = np.array([scales[n, G]], dtype="<u2").view(np.uint8)
+            out[n, b, 8 + 2 * g:10 + 2 * g] = np.array([biases[n, G]], dtype="<u2").view(np.uint8)
+            for l in range(32):
+                lo_k, hi_k = 64 * G + l, 64 * G + 32 + l
+                lo = (int(q[n, lo_k // 8]) >> (4 * (lo_k % 8))) & 15
+                hi = (int(q[n, hi_k // 8]) >> (4 * (hi_k % 8))) & 15
+                out[n, b, 16 + 32 * g + l] = lo | (hi << 4)
+    return out.reshape(-1)

@@ -21,6 +21,7 @@ int oracle_block_bytes(int type)
     case ORACLE_Q4_K: return 2 + 2 + 12 + 128;       /* d, dmin, scales, qs     */
     case ORACLE_Q5_K: return 2 + 2 + 12 + 32 + 128;  /* d, dmin, scales, qh, qs */
     case ORACLE_Q6_K: return 128 + 64 + 16 + 2;      /* ql, qh, scales, d       */
+    case ORACLE_IA4: return 8 + 8 + 128;             /* scales, biases, codes   */
     default: return 0;
     }
 }
@@ -174,6 +175,20 @@ int oracle_pack(int type, const oracle_fields *f, uint8_t *blk)
 
 int oracle_dequant_block_f64(int type, const uint8_t *blk, double w[256])
 {
+    if (type == ORACLE_IA4) {
+        /* group g = weights 64g..64g+63: scale at bytes 2g, bias at 8+2g (bf16);
+         * code byte 16+32g+l holds weight 64g+l (low nibble) and 64g+32+l (high) */
+        for (int g = 0; g < 4; ++g) {
+            double scale = oracle_bf16_to_double(rd16(blk + 2 * g));
+            double bias = oracle_bf16_to_double(rd16(blk + 8 + 2 * g));
+            for (int l = 0; l < 32; ++l) {
+                int byte = blk[16 + 32 * g + l];
+                w[64 * g + l] = scale * (double)(byte & 15) + bias;
+                w[64 * g + 32 + l] = scale * (double)(byte >> 4) + bias;
+            }
+        }
+        return 0;
+    }
     oracle_fields f;
     if (oracle_unpack(type, blk, &f)) return -1;
     double d = oracle_half_to_double(f.d_bits);

@@ -18,6 +18,11 @@
  *   (readings listed in the design notes), and the dequantization formulas
  *     Q4_K, Q5_K:  w = d * sc_j * q - dmin * m_j   (j = 32-weight sub-block)
  *     Q6_K:        w = d * sc_j * (q - 32)        (j = 16-weight sub-block)
+ *   IA4 (group-affine INT4, "ANE Fieldfare" README, "Requirements": an
+ *   mlx-community 4-bit checkpoint; MLX's affine form as read by this
+ *   library): 144-byte blocks of 256 weights, 4 bf16 scales, 4 bf16 biases,
+ *   128 code bytes (byte 32g+l: weight 64g+l low nibble, 64g+32+l high nibble)
+ *     IA4:         w = scale_g * q + bias_g      (g = 64-weight group)
  *
  * Everything is computed in fp64; dequantized values are exact in fp64 for all
  * finite inputs whose fp16 exponents differ by less than ~30 binades, and are
@@ -32,7 +37,7 @@
 extern "C" {
 #endif
 
-enum { ORACLE_Q4_K = 1, ORACLE_Q5_K = 2, ORACLE_Q6_K = 3 };
+enum { ORACLE_Q4_K = 1, ORACLE_Q5_K = 2, ORACLE_Q6_K = 3, ORACLE_IA4 = 4 };
 enum { ORACLE_X_F32 = 0, ORACLE_X_BF16 = 1 };
 
 /* bytes of one 256-weight super-block: 144 / 176 / 210, or 0 for a bad type */

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_block_bytes(L):
-    assert [L.kq_block_bytes(t) for t in (1, 2, 3)] == [144, 176, 210]
+    assert [L.kq_block_bytes(t) for t in (1, 2, 3, 4)] == [144, 176, 210, 144]
     assert L.kq_block_bytes(0) == 0 and L.kq_block_bytes(9) == 0
 
 
@@ -66,7 +66,16 @@ def test_argument_errors_without_gpu(L):
     assert L.kq_dequant_bf16(2, fake, P(0x1008), 256, None) == -5              # out alignment
     assert L.kq_dequant_bf16(2, None, fake, 256, None) == -1                   # null blocks
     assert L.kq_dequant_bf16(3, fake, fake, 0, None) == 0
-    assert L.kq_unpack(4, fake, 1, None, None, None, None, None, None) == -2
+    assert L.kq_unpack(4, fake, 1, None, None, None, None, None, None) == -2   # IA4: no k-quant fields
+    assert L.kq_unpack(5, fake, 1, None, None, None, None, None, None) == -2
+    assert L.kq_matvec(5, fake, fake, 0, fake, 4, 256, 1, None) == -2         # unknown type
+    assert L.kq_ia4_pack(fake, fake, fake, 2, 96, fake, None) == -3           # K % 64
+    assert L.kq_ia4_pack(fake, fake, fake, -1, 64, fake, None) == -1          # N < 0
+    assert L.kq_ia4_pack(fake, fake, fake, 0, 64, fake, None) == 0            # empty: no-op
+    assert L.kq_ia4_pack(None, fake, fake, 2, 64, fake, None) == -1           # null codes
+    assert L.kq_ia4_pack(P(0x1002), fake, fake, 2, 64, fake, None) == -5      # codes alignment
+    assert L.kq_ia4_pack(fake, P(0x1001), fake, 2, 64, fake, None) == -5      # scales alignment
+    assert L.kq_ia4_pack(fake, fake, fake, 2, 64, P(0x1008), None) == -5      # blocks alignment
     assert L.kq_unpack(1, fake, -1, None, None, None, None, None, None) == -1
 
 
@@ -77,6 +86,7 @@ def test_chain_argument_errors_without_gpu(L):
         o.update(kw)
         return o
     assert kq.kq_chain_workspace_size([ops(type=9)]) == 0
+    assert kq.kq_chain_workspace_size([ops(type=4)]) == 0               # IA4 is not taken by chains
     assert kq.kq_chain_workspace_size([ops(K=500)]) == 0
     assert kq.kq_chain_workspace_size([ops(K=16384 + 32)]) == 0
     assert kq.kq_chain_workspace_size([ops(x=0x200008)]) == 0          # x alignment

@@ -33,6 +33,13 @@ MUTANTS = [
     ("abs sum signed", "acc_abs += fabs(t);", "acc_abs += t;"),
     ("gate dropped", "acc += g * p[(m * top_k + t) * N + n];", "acc += p[(m * top_k + t) * N + n];"),
     ("dmin read from d", "f->dmin_bits = rd16(blk + 2);", "f->dmin_bits = rd16(blk);"),
+    ("ia4 bias dropped", "scale * (double)(byte & 15) + bias;", "scale * (double)(byte & 15);"),
+    ("ia4 nibbles swapped", "w[64 * g + 32 + l] = scale * (double)(byte >> 4) + bias;",
+     "w[64 * g + 32 + l] = scale * (double)(byte & 15) + bias;"),
+    ("ia4 bias read from the scales", "oracle_bf16_to_double(rd16(blk + 8 + 2 * g))",
+     "oracle_bf16_to_double(rd16(blk + 2 * g))"),
+    ("ia4 group index", "double scale = oracle_bf16_to_double(rd16(blk + 2 * g));",
+     "double scale = oracle_bf16_to_double(rd16(blk + 2 * (g & 1)));"),
 ]
 
 # every pin, with one set of arguments each
@@ -50,6 +57,8 @@ CHECKS = (
     + [(pins.test_matvec_brute_force, {"qtype": t, "NK": (3, 512)}) for t in (Q4_K, Q5_K, Q6_K)]
     + [(pins.test_matvec_integer_special_case, {"qtype": t, "x_dtype": "f32"}) for t in (Q4_K, Q5_K, Q6_K)]
     + [(pins.test_unpack_matches_bit_reader, {"qtype": t}) for t in (Q4_K, Q5_K, Q6_K)]
+    + [(pins.test_ia4_pack_then_block_decode_equals_mlx_definition, {}), (pins.test_ia4_hand_worked_block, {}),
+       (pins.test_ia4_matvec_reduces_to_dense_integer_product, {})]
 )
 
 

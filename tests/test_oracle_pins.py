@@ -31,7 +31,8 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "han
 def test_block_sizes(orc):
     lib = orc.lib()
     assert [lib.oracle_block_bytes(t) for t in TYPES] == [144, 176, 210]
-    assert lib.oracle_block_bytes(0) == 0 and lib.oracle_block_bytes(4) == 0
+    assert lib.oracle_block_bytes(0) == 0 and lib.oracle_block_bytes(5) == 0
+    assert lib.oracle_block_bytes(4) == 144  # IA4: 4 + 4 bf16 scales and biases, 128 code bytes
     # bits per weight: 4.5, 5.5, 6.5625
     assert [lib.oracle_block_bytes(t) * 8 / 256 for t in TYPES] == [4.5, 5.5, 6.5625]
 
@@ -518,3 +519,56 @@ def test_dequant_f64_is_exact_weights():
         ref = np.concatenate([oracle.dequant_block_f64(qt, b) for b in blocks.reshape(40, -1)])
         assert np.array_equal(w, ref)
         assert np.array_equal(w.astype(np.float32), oracle.dequant(qt, blocks))
+
+
+# ---------------------------------------------------------------- IA4
+def test_ia4_pack_then_block_decode_equals_mlx_definition(orc):
+    """IA4 pin: regrouping MLX's arrays into blocks and decoding the blocks
+    (the C decoder) gives exactly the weights of the MLX definition computed
+    from the arrays themselves (numpy), for ragged K too."""
+    for N, K in ((3, 320), (2, 704), (1, 2816), (4, 64)):
+        q, s, b = synth.gen_ia4_mlx(N, K, synth.rng(140, N, K))
+        blk = orc.ia4_pack(q, s, b, N, K)
+        assert blk.size == N * ((K + 255) // 256) * 144
+        w = orc.dequant_f64(4, blk).reshape(N, -1)
+        assert np.array_equal(w[:, :K], orc.ia4_dequant_mlx(q, s, b, N, K))
+        assert np.array_equal(w.astype(np.float32).reshape(-1), orc.dequant(4, blk))
+        tail = blk.reshape(N, -1, 144)[:, -1]  # groups past K in the last block are all zero
+        for g in range((K % 256) // 64 if K % 256 else 4, 4):
+            assert not tail[:, 2 * g:2 * g + 2].any() and not tail[:, 8 + 2 * g:10 + 2 * g].any()
+            assert not tail[:, 16 + 32 * g:48 + 32 * g].any()
+
+
+def test_ia4_hand_worked_block(orc):
+    """One group by hand: codes k % 16 for k = 0..63, scale 1.0 (bf16 0x3F80),
+    bias -1.0 (0xBF80).  Block byte 16 + l = (l % 16) | ((32 + l) % 16) << 4
+    = 0x11 * (l % 16); weights are (k % 16) - 1."""
+    words = np.array([[sum(((8 * i + j) % 16) << (4 * j) for j in range(8)) for i in range(8)]], dtype=np.uint32)
+    blk = orc.ia4_pack(words, np.array([[0x3F80]], np.uint16), np.array([[0xBF80]], np.uint16), 1, 64)
+    assert list(blk[0:4]) == [0x80, 0x3F, 0, 0] and list(blk[8:12]) == [0x80, 0xBF, 0, 0]
+    assert list(blk[16:48]) == [0x11 * (l % 16) for l in range(32)]
+    assert not blk[48:].any()
+    w = orc.dequant_f64(4, blk)[:64]
+    assert np.array_equal(w, np.array([(k % 16) - 1.0 for k in range(64)]))
+    # closed forms: scale 0 leaves the bias; all codes 15 give 15 s + b
+    blk2 = blk.copy()
+    blk2[0:2] = [0, 0]
+    assert np.all(orc.dequant_f64(4, blk2)[:64] == -1.0)
+    blk3 = blk.copy()
+    blk3[16:48] = 0xFF
+    assert np.all(orc.dequant_f64(4, blk3)[:64] == 14.0)
+
+
+def test_ia4_matvec_reduces_to_dense_integer_product(orc):
+    """With scale 1 and bias 0 everywhere the IA4 product is the integer code
+    matrix times x (numpy, fp64)."""
+    N, K = 5, 512
+    q, _, _ = synth.gen_ia4_mlx(N, K, synth.rng(141))
+    ones = np.full((N, K // 64), 0x3F80, np.uint16)
+    zeros = np.zeros((N, K // 64), np.uint16)
+    blk = orc.ia4_pack(q, ones, zeros, N, K)
+    x = synth.gen_x(2, K, synth.rng(142))
+    codes = orc.ia4_dequant_mlx(q, ones, zeros, N, K)
+    assert np.all((codes == np.round(codes)) & (codes >= 0) & (codes <= 15))
+    y, _ = orc.matvec(4, blk, N, K, x)
+    assert np.allclose(y, x.astype(np.float64) @ codes.T, rtol=1e-13, atol=1e-12)
