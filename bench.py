@@ -242,7 +242,9 @@ def run_single(args):
     from gguf_quant_weight_super_gb300 import build, kq, synth
     build.build()
     spec = args.single.split(":")
-    qt = {"Q4_K": synth.Q4_K, "Q5_K": synth.Q5_K, "Q6_K": synth.Q6_K}[spec[0]]
+    if spec[0] == "moe_ffn":  # moe_ffn:<type>:<M>: one MoE layer's router + expert FFN (128 experts top-8)
+        return run_single_ffn(args, spec)
+    qt = {"Q4_K": synth.Q4_K, "Q5_K": synth.Q5_K, "Q6_K": synth.Q6_K, "IA4": synth.IA4}[spec[0]]
     N, K = (int(v) for v in spec[1].split("x"))
     M = int(spec[2]) if len(spec) > 2 else 1
     xd = spec[3] if len(spec) > 3 else "bf16"
@@ -254,6 +256,33 @@ def run_single(args):
     for _ in range(args.steps):
         kq.kq_matvec(qt, W, x, kq.KQ_BF16 if xd == "bf16" else kq.KQ_F32, y, N, K, M)
     torch.cuda.synchronize()
+    assert kq.kq_device_error() == 0
+    print(json.dumps({"single": args.single, "runs": args.steps, "ok": True}))
+
+
+def run_single_ffn(args, spec):
+    """One MoE layer of the MoE benchmark (router, then the expert FFN's two
+    launches), `--steps` times, eagerly (for profiler captures)."""
+    import torch
+    from gguf_quant_weight_super_gb300 import kq, synth
+    qt = {"Q4_K": synth.Q4_K, "IA4": synth.IA4}[spec[1]]
+    M = int(spec[2]) if len(spec) > 2 else 1
+    E, H, F, SH, top_k = 128, 2816, 704, 2112, 8
+    g = synth.rng(2, M)
+    mats = [torch.from_numpy(synth.gen_matrix(qt, N, K, g)).cuda()
+            for N, K in ((E * F, H), (E * F, H), (E * H, F), (SH, H), (SH, H), (H, SH))]
+    w = kq.ffn_weights(qt, qt, E, kq.KQ_ACT_GELU_TANH, F, mats[0], mats[1], mats[2], SH, mats[3], mats[4], mats[5])
+    logits = torch.from_numpy(synth.gen_logits(M, E, g)).cuda()
+    x = torch.from_numpy(synth.gen_x(M, H, g, "bf16").view(np.int16)).cuda().view(torch.bfloat16)
+    ids = torch.empty((M, top_k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((M, top_k), dtype=torch.float32, device="cuda")
+    y = torch.empty((M, H), dtype=torch.float32, device="cuda")
+    ws = kq.moe_ffn_workspace(H, F, SH, M, top_k, E)
+    for _ in range(args.steps):
+        kq.kq_moe_route(logits, M, E, top_k, ids, gate, None)
+        kq.kq_moe_ffn(w, ids, gate, x, kq.KQ_BF16, y, H, M, top_k, ws, ws.numel())
+    torch.cuda.synchronize()
+    kq.kq_moe_check(ws)
     assert kq.kq_device_error() == 0
     print(json.dumps({"single": args.single, "runs": args.steps, "ok": True}))
 
@@ -468,7 +497,7 @@ def main():
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single", default=None,
-                    help="profiling helper: run one product TYPE:NxK[:M[:f32|bf16]] (e.g. Q4_K:19456x2560) --steps times")
+                    help="profiling helper: run one product TYPE:NxK[:M[:f32|bf16]] (e.g. Q4_K:19456x2560), or one MoE layer moe_ffn:TYPE:M, --steps times")
     ap.add_argument("--workload", default=None, choices=["q4k_4096", "format_sweep", "verify16", "moe", "dequant"],
                     help="time another configuration instead of the dense sweep (one JSON line each)")
     args = ap.parse_args()
