@@ -577,6 +577,19 @@ def main():
     ms = variants[best]
     step_graph = graphs[best]
 
+    # spread of single steps of the best variant (each replay between its own
+    # pair of events, after the timed region; the value above is the mean)
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for a, b in pairs:
+            a.record(stream)
+            step_graph.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    per = sorted(a.elapsed_time(b) for a, b in pairs)
+    pick = lambda q: per[min(len(per) - 1, int(q * len(per)))]  # noqa: E731
+    spread = {"p10": pick(0.1), "p50": pick(0.5), "p90": pick(0.9), "n": len(per)}
+
     # dominant kernel: prog_kernel.  For the chain, one launch is the whole
     # step; for separate launches, the Q4_K products of a step timed alone
     # (same order, same chaining).
@@ -636,7 +649,8 @@ def main():
     if rank == 0:
         gbs = job_gbs(total_bytes, world, ms)
         line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-                "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "warmup": max(3, args.warmup), "ms_per_step": ms, "ms_per_step_spread": spread,
+                "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "u8 codes x bf16 x, int32/fp32 accumulate", "data": "synthetic",
                 "tok_s_equiv": world * 1e3 / ms, "roofline_tok_s_equiv": peak * 1e9 / total_bytes,
                 "frac_of_hbm_peak": gbs / world / peak,
