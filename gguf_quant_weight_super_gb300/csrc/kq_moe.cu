@@ -7,23 +7,28 @@
 // picks 8 of 128 experts; "Speculative decoding": a planning step groups the
 // tokens of a verify block by expert so each expert is read once.
 //
-// One launch, grid (row tile, distinct-expert rank d):
+// One launch, a one-dimensional grid of up to two segments: a shared
+// expert's CTAs (expert FFN only: every token, tiles split by token pairs),
+// then one CTA per (distinct-expert rank d, row tile), rank-major:
 //  * grouping (every CTA, in shared memory): the routed ids are checked
 //    (an id outside [0, n_experts) is recorded in the workspace error word and
 //    its pair dropped), the distinct experts are ranked in ascending id order,
-//    and CTA (tile, d) takes the d-th one, e, with its pairs (token m, slot j)
+//    and CTA (d, tile) takes the d-th one, e, with its pairs (token m, slot j)
 //    in (m, j) order.  The CTAs of tile 0 also write this plan to the
 //    workspace (expert of each rank, offsets, pairs) for inspection;
 //  * the CTA copies its tile of expert e (whole rows, as large as fits in
 //    100 KB: 256, 128 or 64 rows, a quad of lanes per 4, 2 or 1 of them; wider
-//    rows 32 or 16 rows, 2 or 4 quads per row) with one TMA bulk copy, then for
-//    each pair stages that pair's x as block-float limbs and applies the rows
-//    to it with the lane cores of kq_lane.cuh;
-//  * if no routed id is valid at all, the gated outputs are zero (empty sums);
+//    rows 32 or 16 rows, 2 or 4 quads per row) with one TMA bulk copy -- in
+//    gate|up mode the same rows of both matrices, two copies -- then for each
+//    pair stages that pair's x as block-float limbs and applies the rows to it
+//    with the lane cores of kq_lane.cuh (gate|up mode: act(gate) * up);
+//  * if no routed id is valid at all and there is no shared expert, the
+//    gated outputs are zero (empty sums);
 //  * without gate weights the result of pair (m, j) is row j of token m's
 //    output block (y[m][j][n]); with gate weights it goes to the workspace and
-//    the last CTA to finish the tile (arrival counter) writes
-//    y[m][n] = sum_j g[m][j] * part[m][j][n] in slot order (deterministic).
+//    the last CTA to finish each group of rows (arrival counters) writes
+//    y[m][n] = sum_j g[m][j] * part[m][j][n] in slot order, then adds the
+//    shared expert's part (deterministic).
 #include "kq_lane.cuh"
 
 namespace kq {
