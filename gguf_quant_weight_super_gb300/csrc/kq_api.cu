@@ -340,6 +340,11 @@ kq_status kq_moe_ffn(const kq_moe_ffn_weights* w, const int32_t* expert_ids, con
   return cuda_status(e);
 }
 
+kq_status kq_selftest_wait(int kind, int* observed_code, kq_stream_t stream) {
+  if ((kind != 0 && kind != 1) || !observed_code) return KQ_ERR_ARG;
+  return cuda_status(run_selftest_wait(kind, observed_code, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kq_status kq_moe_check(void* workspace, kq_stream_t stream) {
   if (!workspace) return KQ_ERR_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

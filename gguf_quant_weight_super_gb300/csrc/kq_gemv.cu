@@ -155,24 +155,6 @@ __device__ __forceinline__ void produce(const KqOp& o, int tile, int b0, int n, 
   if (len) bulk_g2s_hint(slot + lane * o.srb, src, len, full, pol);
 }
 
-// Grid barrier arrival: a release add (cumulative: it publishes every write
-// the CTA's consumers made before the consumer barrier that precedes it).
-__device__ __forceinline__ void grid_arrive(int* counter) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(counter) : "memory");
-}
-
-// Bounded wait until the grid-wide arrival counter reaches target (acquire
-// loads; the consumer barrier that follows extends the order to the CTA).
-__device__ __forceinline__ bool grid_wait(const int* counter, int target, int* err) {
-  for (uint32_t i = 0; i < (1u << 23); ++i) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
-    if (v >= target) return true;
-  }
-  record_error(err, DEV_ERR_MBAR_TIMEOUT);
-  return false;
-}
-
 struct Ring {
   uint64_t* full;
   uint64_t* empty;

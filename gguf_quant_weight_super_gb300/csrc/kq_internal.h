@@ -97,6 +97,9 @@ bool ffn_supported(int type_gu, int type_dn, int64_t H, int64_t F, int64_t SH, i
 cudaError_t launch_moe_ffn(const FfnWeights& fw, const int32_t* ids, const float* gate, const void* x, int x_bf16,
                            float* y, int64_t H, int M, int top_k, void* ws, cudaStream_t st);
 
+// Bounded-wait self-test (kq_selftest.cu): 0 = mbarrier wait, 1 = grid-barrier wait.
+cudaError_t run_selftest_wait(int kind, int* observed, cudaStream_t st);
+
 // MoE router (kq_route.cu): top-k + softmax over the selected logits, and the
 // grouping plan (written at ws + 256 in kq_moe_matvec's layout when ws is set)
 bool route_supported(int64_t M, int E, int top_k);

@@ -67,9 +67,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the given phase parity; false (and the error word set) on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-  for (uint32_t i = 0; i < kMaxPolls; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, uint32_t max_polls = kMaxPolls) {
+  for (uint32_t i = 0; i < max_polls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
+  record_error(err, DEV_ERR_MBAR_TIMEOUT);
+  return false;
+}
+
+// Grid barrier arrival: a release add (cumulative: it publishes every write
+// the CTA's consumers made before the consumer barrier that precedes it).
+__device__ __forceinline__ void grid_arrive(int* counter) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(counter) : "memory");
+}
+
+// Bounded wait until the grid-wide arrival counter reaches target (acquire
+// loads; the consumer barrier that follows extends the order to the CTA).
+__device__ __forceinline__ bool grid_wait(const int* counter, int target, int* err, uint32_t max_polls = 1u << 23) {
+  for (uint32_t i = 0; i < max_polls; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    if (v >= target) return true;
+  }
   record_error(err, DEV_ERR_MBAR_TIMEOUT);
   return false;
 }

@@ -39,6 +39,7 @@ SIGNATURES = {
     "kq_moe_matvec": (_I, [_I, _P, ctypes.c_int32, _P, _P, _P, _I, _I, _P, _I64, _I64, _I64, ctypes.c_int32,
                            _P, _SZ, _P]),
     "kq_moe_check": (_I, [_P, _P]),
+    "kq_selftest_wait": (_I, [_I, ctypes.POINTER(ctypes.c_int), _P]),
     "kq_moe_ffn_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32]),
     "kq_moe_ffn_offsets": (_I, [_I64, _I64, _I64, _I64, ctypes.c_int32, ctypes.c_int32,
                                 ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]),
@@ -283,6 +284,13 @@ def kq_moe_ffn(weights: KqMoeFfnWeights, expert_ids, gate_w, x, x_dtype, y, H, M
     _check("kq_moe_ffn", lib().kq_moe_ffn(ctypes.cast(ctypes.pointer(weights), ctypes.c_void_p), _ptr(expert_ids),
                                           _ptr(gate_w), _ptr(x), x_dtype, _ptr(y), H, M, top_k, _ptr(workspace),
                                           workspace_bytes, _stream(stream)))
+
+
+def kq_selftest_wait(kind: int, stream=None) -> int:
+    """Run the bounded-wait self-test (0: mbarrier, 1: grid barrier); returns the observed error code."""
+    code = ctypes.c_int(-1)
+    _check("kq_selftest_wait", lib().kq_selftest_wait(kind, ctypes.byref(code), _stream(stream)))
+    return code.value
 
 
 def kq_device_error(clear: bool = False) -> int:

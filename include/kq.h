@@ -268,6 +268,19 @@ kq_status kq_moe_matvec_noalloc(int type, const void *W_experts, int32_t n_exper
                                 int64_t N, int64_t K, int64_t M, int32_t top_k, kq_stream_t stream);
 
 /*
+ * Self-test of the kernels' bounded waits: launches one small kernel whose
+ * wait can never succeed -- kind 0 an mbarrier that no copy completes, kind 1
+ * a grid-barrier counter that no CTA increments -- through the same wait
+ * functions the products use, with a short poll limit (milliseconds).  The
+ * wait gives up, sets a self-test error word (not the library's) and the
+ * kernel returns.  Synchronizes stream; *observed_code receives the code the
+ * wait recorded: 1 (wait timed out) when the mechanism works.  The context
+ * stays usable afterwards.  Errors: KQ_ERR_ARG (kind not 0/1, NULL
+ * observed_code), KQ_ERR_CUDA.
+ */
+kq_status kq_selftest_wait(int kind, int *observed_code, kq_stream_t stream);
+
+/*
  * Synchronize stream and read the workspace's error word: KQ_ERR_DEVICE if a
  * routed id was out of range since the last check (the word is then
  * cleared), else KQ_OK.

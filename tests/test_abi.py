@@ -100,6 +100,12 @@ def test_chain_argument_errors_without_gpu(L):
         kq.kq_chain_prepare([ops()], 0x800010, 1 << 20, plan, stream=0)
 
 
+def test_selftest_argument_errors_without_gpu(L):
+    code = ctypes.c_int(0)
+    assert L.kq_selftest_wait(2, ctypes.byref(code), None) == -1     # unknown kind
+    assert L.kq_selftest_wait(0, None, None) == -1                   # no output
+
+
 def test_route_argument_errors_without_gpu(L):
     P = ctypes.c_void_p
     fake = P(0x1000)
