@@ -38,8 +38,6 @@ using namespace lane;
 namespace {
 
 constexpr int MT_MIN = 16;      // rows per tile at the most quads per row (sizes the tile counters)
-constexpr int kForcePhases = 0; // 0: quads per row chosen per shape
-constexpr int kForceRows = 0;   // 0: rows per quad chosen per shape
 constexpr int MW = 8;           // warps
 constexpr int MTH = MW * 32;
 constexpr int kMaxPairs = 512;  // M * top_k
@@ -396,8 +394,6 @@ void moe_tile_shape(int64_t row_bytes, int& nph, int& rq) {
   for (int r = 4; r >= 1; r >>= 1)
     if (8 * MW * r * row_bytes + 32 <= kMaxTileBytes) { nph = 1; rq = r; break; }
   if (nph == 4 && 8 * MW / 2 * row_bytes + 32 <= kMaxTileBytes) nph = 2;
-  if (kForcePhases) nph = kForcePhases;
-  if (kForceRows) rq = kForceRows;
   if (nph > 1) rq = 1;
 }
 
