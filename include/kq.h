@@ -103,7 +103,8 @@ kq_status kq_ia4_pack(const uint32_t *q, const uint16_t *scales, const uint16_t 
 
 /*
  * Integer fields of n_blocks consecutive blocks (the super-block unpacker the
- * products use, exposed for inspection).  Any output may be NULL.
+ * products use, exposed for inspection).  Any output may be NULL.  k-quant
+ * types only (KQ_IA4 blocks have no such fields: KQ_ERR_TYPE).
  *   codes     [n_blocks][256] uint8: q (Q4_K 0..15, Q5_K 0..31, Q6_K 0..63, unbiased)
  *   scales    [n_blocks][16]  int8 : Q4_K/Q5_K sc_0..sc_7 (0..63, entries 8..15
  *                                    untouched); Q6_K sc_0..sc_15 (-128..127)
@@ -168,7 +169,7 @@ kq_status kq_matvec(int type, const void *W, const void *x, int x_dtype, float *
  * partial sums; two runs must not use one workspace at the same time.
  */
 typedef struct kq_op {
-  int32_t type;          /* KQ_Q4_K, KQ_Q5_K or KQ_Q6_K                         */
+  int32_t type;          /* KQ_Q4_K, KQ_Q5_K or KQ_Q6_K (not KQ_IA4)            */
   int32_t x_dtype;       /* KQ_F32 or KQ_BF16                                   */
   int32_t wait_previous; /* nonzero: start after all earlier ops have finished  */
   int32_t reserved;      /* must be 0                                           */
