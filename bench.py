@@ -112,6 +112,30 @@ def make_chain(kq, mats, xs, only_type=None):
     return kq.Chain(ops)
 
 
+def device_info(torch) -> dict:
+    """GPU name, SM count, L2 bytes, CUDA runtime and driver versions, host
+    cores (what a measurement was taken on); fields it cannot read are left out."""
+    info = {"host_cores": os.cpu_count()}
+    try:
+        p = torch.cuda.get_device_properties(torch.cuda.current_device())
+        info["name"] = p.name
+        info["sms"] = p.multi_processor_count
+        l2 = getattr(p, "L2_cache_size", None)
+        if l2:
+            info["l2_bytes"] = int(l2)
+        info["cuda"] = torch.version.cuda
+    except Exception:
+        pass
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=10)
+        if out.returncode == 0 and out.stdout.strip():
+            info["driver"] = out.stdout.strip().splitlines()[0]
+    except Exception:
+        pass
+    return info
+
+
 def capture(torch, fn, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -669,7 +693,7 @@ def main():
                 "e2e": {"value": total_bytes * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "gpu_launches": launches[best] * args.steps,
-                "clocks": clk.summary()}
+                "clocks": clk.summary(), "device": device_info(torch)}
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
