@@ -174,3 +174,33 @@ def test_moe_argument_errors_without_gpu(L):
     assert call(wsb=100) == -7
     assert L.kq_moe_workspace_size(704, 1, 8, 128) > 0
     assert L.kq_moe_workspace_size(704, 100, 8, 128) == 0
+
+
+def test_header_is_plain_c_and_links(L, tmp_path):
+    """include/kq.h compiles as C99 and a C program links against libkq.so and
+    calls it (argument-error paths only: no CUDA call is made)."""
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_kq.c"
+    src.write_text(
+        '#include "kq.h"\n'
+        "#include <stdio.h>\n"
+        "int main(void) {\n"
+        "  kq_moe_ffn_weights w = {0};\n"
+        "  int code = 0;\n"
+        "  if (kq_block_bytes(KQ_Q4_K) != 144 || kq_block_bytes(KQ_IA4) != 144) return 1;\n"
+        "  if (kq_matvec(KQ_Q6_K, 0, 0, KQ_BF16, 0, 4, 250, 1, 0) != KQ_ERR_SHAPE) return 2;\n"
+        "  if (kq_moe_ffn(&w, 0, 0, 0, KQ_F32, 0, 512, 2, 4, 0, 0, 0) != KQ_ERR_TYPE) return 3;\n"
+        "  if (kq_selftest_wait(7, &code, 0) != KQ_ERR_ARG) return 4;\n"
+        "  printf(\"%s\\n\", kq_status_string(KQ_ERR_WORKSPACE));\n"
+        "  return 0;\n"
+        "}\n")
+    exe = tmp_path / "use_kq"
+    libdir = os.path.dirname(kq.LIB_PATH)
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                           "-o", str(exe), "-L", libdir, "-lkq", "-Wl,-rpath," + libdir])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    assert out.stdout.strip()
