@@ -16,9 +16,10 @@
 //    a ring of S shared-memory stages that it fills with 1-D TMA bulk copies
 //    of its units' row segments (Q6_K's 210-byte blocks are fetched as the
 //    16-byte aligned superset and addressed at their true offset);
-//  * x (fp32) and the sums of each part-length run of x live in shared memory;
-//    lanes turn codes into floats 1 + q/2^s with one byte-permute each and
-//    accumulate with packed fp32x2 FMAs (see kq_decode.cuh for the algebra);
+//  * x (fp32) lives in shared memory; lanes turn codes into floats
+//    f = 1 + q/2^s with one byte-permute each, form every weight exactly
+//    rounded, w = (f - 1) 2^s d sc - dmin m (f - 1 is exact), and accumulate
+//    w x with packed fp32x2 FMAs;
 //  * K-range partial sums of a tile are combined, in range order, by the last
 //    warp of the CTA to finish one of that tile's units;
 //  * weight tiles are requested before griddepcontrol.wait, so under
@@ -164,10 +165,15 @@ __device__ __forceinline__ void issue_job(const GemvArgs& a, int64_t tile, int b
     if (i < nrows) bulk_g2s(slot + i * a.slot_row_bytes, src[i], len[i], bar);
 }
 
-// Pre-bytes -> 4 floats -> two fp32x2 FMAs against 4 consecutive x values.
-__device__ __forceinline__ float2 fma4(uint32_t pre, const float4& xv, float2 s) {
-  s = ffma2(make_float2(byte_to_f(pre, 0), byte_to_f(pre, 1)), make_float2(xv.x, xv.y), s);
-  s = ffma2(make_float2(byte_to_f(pre, 2), byte_to_f(pre, 3)), make_float2(xv.z, xv.w), s);
+// Pre-bytes -> 4 weights -> two fp32x2 FMAs against 4 consecutive x values.
+// f = 1 + q/2^k, so f - 1 is exact and w = (f - 1) A - Mm (A = 2^k d sc,
+// Mm = dmin m, or 32 d sc for Q6_K) is the exact weight rounded once.
+__device__ __forceinline__ float2 fma4(uint32_t pre, const float4& xv, float2 a, float2 mm, float2 s) {
+  const float2 one = make_float2(-1.0f, -1.0f);
+  const float2 w01 = ffma2(fadd2(make_float2(byte_to_f(pre, 0), byte_to_f(pre, 1)), one), a, mm);
+  const float2 w23 = ffma2(fadd2(make_float2(byte_to_f(pre, 2), byte_to_f(pre, 3)), one), a, mm);
+  s = ffma2(w01, make_float2(xv.x, xv.y), s);
+  s = ffma2(w23, make_float2(xv.z, xv.w), s);
   return s;
 }
 
@@ -198,12 +204,15 @@ __device__ __forceinline__ uint4 lds16_a2(const uint8_t* p) {
                     __funnelshift_r(w3, w4, sh));
 }
 
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
   return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
 
 // One block of R rows for quad lane c; `rem` = weights of the block inside K.
-// acc[i][m] += A_p * sum_{part p} f*x + B_p * sum_{part p} x, over the lane's parts.
+// acc[i][m] += sum_{part p} w*x over the lane's parts, each weight the exactly
+// rounded fp32 value (parts past K have zero weights).
 template <int QT, int R, int MT>
 __device__ __forceinline__ void do_block(const uint8_t* const (&blk)[R], const bool (&rok)[R], int c, int rem,
                                          const float* xb, const float* Xb, int xstride, int Xstride, int M,
@@ -225,13 +234,13 @@ __device__ __forceinline__ void do_block(const uint8_t* const (&blk)[R], const b
       const uint2 s = ld8_a2(b + 192 + 8 * h + (c & 1));
       const uint32_t se = __byte_perm(s.x, s.y, 0x6420);
       const float d = half_bits_to_float(reinterpret_cast<const uint16_t*>(b + 208)[0]);
-      const float dA = 128.0f * d, dB = -160.0f * d;
+      const float dA = 128.0f * d, dB = -32.0f * d;
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
         const float sc = static_cast<float>(static_cast<int8_t>((se >> (8 * p)) & 0xFF));
         const bool ok = qpos<QT>(c, p) + PL <= rem;
         A[i][p] = ok ? dA * sc : 0.0f;
-        B[i][p] = ok ? dB * sc : 0.0f;
+        B[i][p] = ok ? dB * sc : 0.0f;  // minus the subtracted constant
       }
     } else {
       const uint4 hdr = *reinterpret_cast<const uint4*>(b);
@@ -253,7 +262,7 @@ __device__ __forceinline__ void do_block(const uint8_t* const (&blk)[R], const b
         const float mm = dmin * static_cast<float>((v >> (16 + 8 * p)) & 0xFF);
         const bool ok = qpos<QT>(c, p) + PL <= rem;
         A[i][p] = ok ? av : 0.0f;
-        B[i][p] = ok ? -(av + mm) : 0.0f;
+        B[i][p] = ok ? -mm : 0.0f;
       }
     }
   }
@@ -261,7 +270,6 @@ __device__ __forceinline__ void do_block(const uint8_t* const (&blk)[R], const b
   for (int m = 0; m < MT; ++m) {
     if (m >= M) break;
     const float* xm = xb + m * xstride;
-    const float* Xm = Xb + m * Xstride;
     float2 Sx[R][P];
 #pragma unroll
     for (int i = 0; i < R; ++i)
@@ -277,10 +285,10 @@ __device__ __forceinline__ void do_block(const uint8_t* const (&blk)[R], const b
         for (int i = 0; i < R; ++i) {
           if (!rok[i]) continue;
           const uint32_t a = word_of(raw[i][0], w), bq = word_of(raw[i][1], w), h = word_of(raw[i][2], w);
-          Sx[i][0] = fma4(q6_t0(a, h), xv[0], Sx[i][0]);
-          Sx[i][1] = fma4(q6_t1(bq, h), xv[1], Sx[i][1]);
-          Sx[i][2] = fma4(q6_t2(a, h), xv[2], Sx[i][2]);
-          Sx[i][3] = fma4(q6_t3(bq, h), xv[3], Sx[i][3]);
+          Sx[i][0] = fma4(q6_t0(a, h), xv[0], f2(A[i][0]), f2(B[i][0]), Sx[i][0]);
+          Sx[i][1] = fma4(q6_t1(bq, h), xv[1], f2(A[i][1]), f2(B[i][1]), Sx[i][1]);
+          Sx[i][2] = fma4(q6_t2(a, h), xv[2], f2(A[i][2]), f2(B[i][2]), Sx[i][2]);
+          Sx[i][3] = fma4(q6_t3(bq, h), xv[3], f2(A[i][3]), f2(B[i][3]), Sx[i][3]);
         }
       }
     } else {
@@ -294,12 +302,12 @@ __device__ __forceinline__ void do_block(const uint8_t* const (&blk)[R], const b
           if (!rok[i]) continue;
           const uint32_t q = word_of(raw[i][w >> 2], w & 3);
           if constexpr (kQ4Codes<QT>) {
-            Sx[i][0] = fma4(q4_lo(q), xlo, Sx[i][0]);
-            Sx[i][1] = fma4(q4_hi(q), xhi, Sx[i][1]);
+            Sx[i][0] = fma4(q4_lo(q), xlo, f2(A[i][0]), f2(B[i][0]), Sx[i][0]);
+            Sx[i][1] = fma4(q4_hi(q), xhi, f2(A[i][1]), f2(B[i][1]), Sx[i][1]);
           } else {
             const uint32_t hb = word_of(raw[i][2 + (w >> 2)], w & 3);
-            Sx[i][0] = fma4(q5_lo(q, hb, c), xlo, Sx[i][0]);
-            Sx[i][1] = fma4(q5_hi(q, hb, c), xhi, Sx[i][1]);
+            Sx[i][0] = fma4(q5_lo(q, hb, c), xlo, f2(A[i][0]), f2(B[i][0]), Sx[i][0]);
+            Sx[i][1] = fma4(q5_hi(q, hb, c), xhi, f2(A[i][1]), f2(B[i][1]), Sx[i][1]);
           }
         }
       }
@@ -308,11 +316,7 @@ __device__ __forceinline__ void do_block(const uint8_t* const (&blk)[R], const b
     for (int i = 0; i < R; ++i) {
       if (!rok[i]) continue;
 #pragma unroll
-      for (int p = 0; p < P; ++p) acc[i][m] = ffma2(make_float2(A[i][p], A[i][p]), Sx[i][p], acc[i][m]);
-#pragma unroll
-      for (int p = 0; p < P; p += 2)
-        acc[i][m] = ffma2(make_float2(B[i][p], B[i][p + 1]),
-                          make_float2(Xm[qpos<QT>(c, p) / PL], Xm[qpos<QT>(c, p + 1) / PL]), acc[i][m]);
+      for (int p = 0; p < P; ++p) acc[i][m] = fadd2(acc[i][m], Sx[i][p]);
     }
   }
 }

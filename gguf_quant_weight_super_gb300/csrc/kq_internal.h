@@ -24,15 +24,11 @@ GemvPlan plan_gemv_batched(int qtype, int64_t N, int K, int M);
 // M >= 1 tokens, x staged in shared memory windows (kq_gemv_batched.cu)
 cudaError_t launch_gemv_batched(int qtype, const void* W, const void* x, int x_bf16, float* y, int64_t N, int K,
                                 int M, cudaStream_t stream, bool pdl);
-// one token, x held in registers per quad (kq_gemv1.cu); returns
-// cudaErrorNotSupported when the shape is outside its limits
-cudaError_t launch_gemv1(int qtype, const void* W, const void* x, int x_bf16, float* y, int64_t N, int K,
-                         cudaStream_t stream, bool pdl);
 
 // One-token products (kq_gemv.cu): a single product, or a program of
 // products run by one persistent launch with grid-wide ordering between
 // dependent ones and split-K partial sums in the program's workspace.
-// (M tokens: 1, or 2 with bf16 x; y is [M][N])
+// (M tokens: 1, or 2..4 with bf16 x; y is [M][N])
 cudaError_t launch_matvec1(int qtype, const void* W, const void* x, int x_bf16, float* y, int64_t N, int K,
                            cudaStream_t stream, bool pdl, int M = 1);
 struct ProgOpDesc {
@@ -43,10 +39,10 @@ struct ProgOpDesc {
   int64_t N, K;
 };
 struct ProgPlan {
-  int n_ops, nb_max, nl_max, S, slot;
+  int n_ops, nb_max, nimg, S, slot;  // nimg: x images in shared memory (2 when an op has fp32 x)
   int coop;       // grid barriers: cooperative launch
   int final_fix;  // split-K sums remain after the last op
-  int nl_min;     // x limbs of the op with the fewest (equal to nl_max: one x dtype)
+  int xk;         // x dtypes of the ops: 1 all bf16, 2 all fp32, 0 both
   int64_t smem, ws_bytes;
 };
 // workspace bytes of a program (0: some op cannot run on this path)

@@ -80,9 +80,9 @@ struct MoeArgs {
 };
 
 struct MoeSmem {
-  int ids[kMaxPairs];
+  int16_t ids[kMaxPairs];    // validated expert ids (-1: dropped)
   uint32_t bits[kMaxExperts / 32];
-  int pairs[kMaxPairs];
+  int16_t pairs[kMaxPairs];  // this CTA's pairs (routed) or tokens (shared)
   int misc[8];  // 0: e, 1: D, 2: np, 3: offset of e, 4: valid pairs, 5: groups this CTA combines
 };
 
@@ -91,33 +91,24 @@ __host__ __device__ inline size_t moe_ximg_offset() { return (sizeof(MoeSmem) + 
 // Row sums of one pair over the tile for the RQ rows of this quad (rows
 // rp, rp + rstride, ...; nph quads per row, the quad of phase ph taking blocks
 // ph, ph + nph, ...): each block's x slice is loaded once for all RQ rows.
-template <int QT, int NL, int RQ>
-__device__ __forceinline__ void pair_rows(uint32_t rp, uint32_t rstride, int nb, const XImg& xi, int ph, int nph,
-                                          int c, const ScaleLane& sl, float (&acc)[4]) {
+// NI x images (fp32 x: hi and lo) add into the same sums.
+template <int QT, int NI, int RQ>
+__device__ __forceinline__ void pair_rows(uint32_t rp, uint32_t rstride, int nb, const XImg (&xs)[NI], int ph,
+                                          int nph, int c, const ScaleLane& sl, float (&acc)[4]) {
   constexpr int BB = Fmt<QT>::BYTES;
-  const int xoff = (QT == T_Q6_K) ? (40 * (c >> 1) + 4 * (c & 1)) : 20 * c;
+  float a[RQ];
 #pragma unroll
-  for (int i = 0; i < RQ; ++i) acc[i] = 0.0f;
+  for (int i = 0; i < RQ; ++i) a[i] = 0.0f;
   for (int b = ph; b < nb; b += nph) {
-    XSlice<NL> X;
-    load_slice<QT, NL>(xi.limb_s + 4 * (b * XWB + xoff), 4 * xi.plane, X);
-    const float s = __uint_as_float(lds32(xi.scale_s + 4 * (2 * b + (c >> 1))));
-    if constexpr (QT == T_Q6_K) {
-      const uint4 sv = lds128(xi.si16q_s + 4 * (16 * b + 4 * c));
-      const int4 si = make_int4(static_cast<int>(sv.x), static_cast<int>(sv.y), static_cast<int>(sv.z),
-                                static_cast<int>(sv.w));
+    uint32_t rb[RQ];
 #pragma unroll
-      for (int i = 0; i < RQ; ++i) acc[i] = core_q6<NL>(rp + i * rstride + b * BB, X, si, s, c, acc[i]);
-    } else {
-      const uint2 sv = lds64(xi.si32_s + 4 * (8 * b + 2 * c));
-      const int2 si = make_int2(static_cast<int>(sv.x), static_cast<int>(sv.y));
+    for (int i = 0; i < RQ; ++i) rb[i] = rp + i * rstride + b * BB;
 #pragma unroll
-      for (int i = 0; i < RQ; ++i) acc[i] = core_q45<QT, NL>(rp + i * rstride + b * BB, X, si, s, c, sl, acc[i]);
-    }
+    for (int t = 0; t < NI; ++t) block_rows<QT, RQ>(xs[t], b, rb, c, sl, a);
   }
 #pragma unroll
   for (int i = 0; i < RQ; ++i) {
-    float v = acc[i];
+    float v = a[i];
     v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
     v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
     for (int o = 4; o < 4 * nph; o <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -133,7 +124,7 @@ __device__ __forceinline__ float ffn_act(int act, float g) {
   return g / (1.0f + expf(-g));
 }
 
-template <int QT, int NL>
+template <int QT, int XK>
 __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   MoeSmem& sm = *reinterpret_cast<MoeSmem*>(smem + 16);
@@ -152,8 +143,11 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
   const int MK = a.M * a.top_k;
   int nb_max = a.seg[0].nb;
   if (a.nseg > 1 && a.seg[1].nb > nb_max) nb_max = a.seg[1].nb;
-  const XImg xi = ximg_at(smem + moe_ximg_offset(), sg.nb, NL);
-  uint8_t* tile_buf = smem + moe_ximg_offset() + ((ximg_bytes(nb_max, NL) + 127) & ~size_t(127));
+  constexpr int NI = XK == 2 ? 2 : 1;  // fp32 x: hi and lo images
+  XImg xs[NI];
+#pragma unroll
+  for (int t = 0; t < NI; ++t) xs[t] = ximg_at(smem + moe_ximg_offset() + t * ximg_bytes(nb_max), sg.nb);
+  uint8_t* tile_buf = smem + moe_ximg_offset() + ((NI * ximg_bytes(nb_max) + 127) & ~size_t(127));
 
   // ---- grouping: validated ids, presence bits, the d-th distinct expert
   auto group = [&]() {
@@ -169,7 +163,7 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
       } else {
         atomicOr(&sm.bits[id >> 5], 1u << (id & 31));
       }
-      sm.ids[i] = id;
+      sm.ids[i] = static_cast<int16_t>(id);
     }
     __syncthreads();
     if (warp == 0) {
@@ -256,7 +250,7 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
   // ---- the pairs in (m, slot) order (routed), or this CTA's tokens (shared)
   if (shared_seg) {
     const int nt = static_cast<int>(min_i64(kSharedTokens, a.M - tok0));
-    if (tid < nt) sm.pairs[tid] = tok0 + tid;
+    if (tid < nt) sm.pairs[tid] = static_cast<int16_t>(tok0 + tid);
     if (tid == 0) sm.misc[2] = nt;
   } else if (warp == 0) {
     int np = 0, below = 0, valid = 0;
@@ -264,7 +258,7 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
       const int i = i0 + lane;
       const int id = i < MK ? sm.ids[i] : -1;
       const uint32_t mine = __ballot_sync(0xFFFFFFFFu, id == e);
-      if (id == e) sm.pairs[np + __popc(mine & ((1u << lane) - 1))] = i;
+      if (id == e) sm.pairs[np + __popc(mine & ((1u << lane) - 1))] = static_cast<int16_t>(i);
       np += __popc(mine);
       below += __popc(__ballot_sync(0xFFFFFFFFu, id >= 0 && id < e));
       valid += __popc(__ballot_sync(0xFFFFFFFFu, id >= 0));
@@ -296,20 +290,20 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
     const int pr = sm.pairs[j];
     const int m = shared_seg ? pr : pr / a.top_k;
     const int64_t xrow = (!shared_seg && sg.x_per_slot) ? pr : m;
-    const void* xp = a.x_bf16 ? static_cast<const void*>(static_cast<const uint16_t*>(sg.x) + xrow * sg.K)
-                              : static_cast<const void*>(static_cast<const float*>(sg.x) + xrow * sg.K);
+    const void* xp = XK == 1 ? static_cast<const void*>(static_cast<const uint16_t*>(sg.x) + xrow * sg.K)
+                             : static_cast<const void*>(static_cast<const float*>(sg.x) + xrow * sg.K);
     __syncthreads();  // the previous pair is done with the x image
-    stage_x<NL, MTH>(xp, NL == 2, sg.K, sg.nb, xi, tid);
+    stage_x<MTH>(xp, XK == 1, sg.K, sg.nb, xs[0], xs[NI - 1], tid);
     __syncthreads();
     if (j == 0) ok = mbar_wait(bar, 0, a.err);
     float v[4], u[4];
-    if (sg.rq == 4) pair_rows<QT, NL, 4>(rp, rstride, sg.nb, xi, ph, sg.nph, c, sl, v);
-    else if (sg.rq == 2) pair_rows<QT, NL, 2>(rp, rstride, sg.nb, xi, ph, sg.nph, c, sl, v);
-    else pair_rows<QT, NL, 1>(rp, rstride, sg.nb, xi, ph, sg.nph, c, sl, v);
+    if (sg.rq == 4) pair_rows<QT, NI, 4>(rp, rstride, sg.nb, xs, ph, sg.nph, c, sl, v);
+    else if (sg.rq == 2) pair_rows<QT, NI, 2>(rp, rstride, sg.nb, xs, ph, sg.nph, c, sl, v);
+    else pair_rows<QT, NI, 1>(rp, rstride, sg.nb, xs, ph, sg.nph, c, sl, v);
     if (a.gu) {
-      if (sg.rq == 4) pair_rows<QT, NL, 4>(rp2, rstride, sg.nb, xi, ph, sg.nph, c, sl, u);
-      else if (sg.rq == 2) pair_rows<QT, NL, 2>(rp2, rstride, sg.nb, xi, ph, sg.nph, c, sl, u);
-      else pair_rows<QT, NL, 1>(rp2, rstride, sg.nb, xi, ph, sg.nph, c, sl, u);
+      if (sg.rq == 4) pair_rows<QT, NI, 4>(rp2, rstride, sg.nb, xs, ph, sg.nph, c, sl, u);
+      else if (sg.rq == 2) pair_rows<QT, NI, 2>(rp2, rstride, sg.nb, xs, ph, sg.nph, c, sl, u);
+      else pair_rows<QT, NI, 1>(rp2, rstride, sg.nb, xs, ph, sg.nph, c, sl, u);
 #pragma unroll
       for (int i = 0; i < 4; ++i) v[i] = ffn_act(a.act, v[i]) * u[i];
     }
@@ -339,7 +333,7 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
     const int m = i / nrows, r = i - m * nrows;
     if (!((mine >> (r / a.G)) & 1)) continue;
     const float* pp = part + static_cast<int64_t>(m) * a.top_k * sg.N + r0 + r;
-    const int* id = sm.ids + m * a.top_k;
+    const int16_t* id = sm.ids + m * a.top_k;
     const float* g = a.gate + m * a.top_k;
     float v = 0.0f;
     int j = 0;
@@ -359,12 +353,12 @@ __global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArg
   if (tid < ng && ((mine >> tid) & 1)) a.cnt[g0 + tid] = 0;  // ready for the next call
 }
 
-template <int QT, int NL>
+template <int QT, int XK>
 cudaError_t launch_moe_t(const MoeArgs& a, size_t smem, cudaStream_t st) {
   static bool smem_set[64] = {false};
   const int dev = current_device_id();
   if (!smem_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(moe_kernel<QT, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(moe_kernel<QT, XK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kMaxSmemPerBlock);
     if (e != cudaSuccess) return e;
     smem_set[dev] = true;
@@ -379,7 +373,7 @@ cudaError_t launch_moe_t(const MoeArgs& a, size_t smem, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_kernel<QT, NL>, a);
+  return cudaLaunchKernelEx(&cfg, moe_kernel<QT, XK>, a);
 }
 
 size_t a256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -443,24 +437,24 @@ size_t seg_tile_bytes(const MoeSeg& s) {
 }
 
 cudaError_t launch_args(MoeArgs& a, int qtype, cudaStream_t st) {
-  const int NL = a.x_bf16 ? 2 : 3;
+  const int XK = a.x_bf16 ? 1 : 2, NI = a.x_bf16 ? 1 : 2;
   int nb = a.seg[0].nb;
   size_t tb = seg_tile_bytes(a.seg[0]);
   if (a.nseg > 1) {
     nb = nb > a.seg[1].nb ? nb : a.seg[1].nb;
     tb = tb > seg_tile_bytes(a.seg[1]) ? tb : seg_tile_bytes(a.seg[1]);
   }
-  const size_t smem = moe_ximg_offset() + ((ximg_bytes(nb, NL) + 127) & ~size_t(127)) + tb;
+  const size_t smem = moe_ximg_offset() + ((NI * ximg_bytes(nb) + 127) & ~size_t(127)) + tb;
   if (smem > static_cast<size_t>(kMaxSmemPerBlock)) return cudaErrorNotSupported;
-  switch (qtype * 4 + NL) {
+  switch (qtype * 4 + XK) {
+    case T_Q4_K * 4 + 1: return launch_moe_t<T_Q4_K, 1>(a, smem, st);
     case T_Q4_K * 4 + 2: return launch_moe_t<T_Q4_K, 2>(a, smem, st);
-    case T_Q4_K * 4 + 3: return launch_moe_t<T_Q4_K, 3>(a, smem, st);
+    case T_Q5_K * 4 + 1: return launch_moe_t<T_Q5_K, 1>(a, smem, st);
     case T_Q5_K * 4 + 2: return launch_moe_t<T_Q5_K, 2>(a, smem, st);
-    case T_Q5_K * 4 + 3: return launch_moe_t<T_Q5_K, 3>(a, smem, st);
+    case T_Q6_K * 4 + 1: return launch_moe_t<T_Q6_K, 1>(a, smem, st);
     case T_Q6_K * 4 + 2: return launch_moe_t<T_Q6_K, 2>(a, smem, st);
-    case T_Q6_K * 4 + 3: return launch_moe_t<T_Q6_K, 3>(a, smem, st);
+    case T_IA4 * 4 + 1: return launch_moe_t<T_IA4, 1>(a, smem, st);
     case T_IA4 * 4 + 2: return launch_moe_t<T_IA4, 2>(a, smem, st);
-    case T_IA4 * 4 + 3: return launch_moe_t<T_IA4, 3>(a, smem, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -586,11 +580,12 @@ cudaError_t launch_moe(int qtype, const void* W, int n_experts, const int32_t* i
 // device array instead of a caller workspace.  For callers that cannot
 // allocate device memory at all -- a plain C host embedding libkq with no
 // device allocator of its own, or a decode loop that must not allocate -- and
-// so cannot provide the workspace kq_moe_matvec needs.  The array is zero at
-// module load; the arrival counters return to zero after every call; bad ids
-// are reported in the library's device error word (kq_device_error).  One
-// array per device: calls that overlap in time (any stream, any host thread)
-// race on it and must not be issued.
+// so cannot provide the workspace kq_moe_matvec needs.  The array keeps what
+// the last call left; its layout depends on the call's shape, so a gated call
+// first clears its own arrival counters (one stream-ordered memset, no
+// allocation).  Bad ids are reported in the library's device error word
+// (kq_device_error).  One array per device: calls that overlap in time (any
+// stream, any host thread) race on it and must not be issued.
 // ---------------------------------------------------------------------------
 namespace {
 constexpr size_t kMoeStaticScratch = 2u << 20;  // bytes: M*top_k*N <= ~500K outputs
@@ -603,13 +598,18 @@ size_t moe_static_scratch_bytes() { return kMoeStaticScratch; }
 cudaError_t launch_moe_static(int qtype, const void* W, int n_experts, const int32_t* ids, const float* gate,
                               const void* x, int x_bf16, int x_per_slot, float* y, int64_t N, int K, int M,
                               int top_k, cudaStream_t st) {
-  if (moe_layout(N, M, top_k, n_experts).bytes > kMoeStaticScratch) return cudaErrorInvalidValue;
+  const MoeLayout L = moe_layout(N, M, top_k, n_experts);
+  if (L.bytes > kMoeStaticScratch) return cudaErrorInvalidValue;
   const int dev = current_device_id();
   if (!g_moe_scratch_ptr[dev]) {  // once per device, with that device current
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_moe_scratch);
     if (e != cudaSuccess) return e;
     g_moe_scratch_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  if (gate) {  // the counters of this shape start at zero whatever an earlier call of another shape left there
+    const cudaError_t e = cudaMemsetAsync(g_moe_scratch_ptr[dev] + L.cnt_off, 0, sizeof(int) * L.ntiles, st);
+    if (e != cudaSuccess) return e;
   }
   return launch_moe_err(qtype, W, n_experts, ids, gate, x, x_bf16, x_per_slot, y, N, K, M, top_k,
                         g_moe_scratch_ptr[dev], device_error_ptr(), st);

@@ -95,14 +95,34 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // Four weights (bytes t = 0..3 of v, placed at byte position pos) as two
-// packed bf16 pairs: w = f * A + C.
-__device__ __forceinline__ void four_weights(uint32_t v, int pos, float A, float C, uint32_t& p0, uint32_t& p1) {
-  const float2 a = make_float2(A, A), c = make_float2(C, C);
-  const float2 f01 = make_float2(byte_float(v, 0, pos), byte_float(v, 1, pos));
-  const float2 f23 = make_float2(byte_float(v, 2, pos), byte_float(v, 3, pos));
+// packed bf16 pairs.  With f = 0.5 + q/2^k and A = 2^k d sc the weight is
+// w = f A - (A/2 + Mt) (Mt = dmin m; 0 for Q6_K's offset form).  When
+// A/2 + Mt is exact in fp32 (exact_c) that is one fma, rounded once;
+// otherwise (d and dmin far apart in exponent) w = (f - 0.5) A - Mt, where
+// f - 0.5 = q/2^k is exact: rounded once as well.  Then one rounding to bf16.
+__device__ __forceinline__ void four_weights(uint32_t v, int pos, float A, float Mt, bool exact_c, uint32_t& p0,
+                                             uint32_t& p1) {
+  const float2 a = make_float2(A, A);
+  float2 f01 = make_float2(byte_float(v, 0, pos), byte_float(v, 1, pos));
+  float2 f23 = make_float2(byte_float(v, 2, pos), byte_float(v, 3, pos));
+  float2 c;
+  if (exact_c) {
+    const float C = -(0.5f * A + Mt);
+    c = make_float2(C, C);
+  } else {
+    const float2 h = make_float2(-0.5f, -0.5f);
+    f01 = fadd2(f01, h);
+    f23 = fadd2(f23, h);
+    c = make_float2(-Mt, -Mt);
+  }
   const float2 w01 = ffma2(f01, a, c), w23 = ffma2(f23, a, c);
   p0 = pack_bf16(w01.x, w01.y);
   p1 = pack_bf16(w23.x, w23.y);
+}
+// Whether a + b is exact in fp32 (the TwoSum error term is zero).
+__device__ __forceinline__ bool sum_exact(float a, float b) {
+  const float s = __fadd_rn(a, b), bb = __fsub_rn(s, a), aa = __fsub_rn(s, bb);
+  return __fadd_rn(__fsub_rn(a, aa), __fsub_rn(b, bb)) == 0.0f;
 }
 
 // Half g (weights 128g .. 128g+127) of the block at bp (shared address) of
@@ -139,6 +159,9 @@ __device__ __forceinline__ void dequant_half(uint32_t bp, int g, uint32_t taddr)
         dmh = dmin * static_cast<float>((mb >> (16 * cc + 8)) & 0xFF);
       }
       const uint4 qa = lds128(bp + QS + 32 * c), qb = lds128(bp + QS + 32 * c + 16);
+      // Q4_K high nibbles sit at byte position 1 (f = 0.5 + q/4096): A = 4096 d sc
+      const float Al = 256.0f * dsl, Ah = (kQ4Codes<QT> ? 4096.0f : 256.0f) * dsh;
+      const bool exl = sum_exact(0.5f * Al, dml), exh = sum_exact(0.5f * Ah, dmh);
 #pragma unroll
       for (int part = 0; part < 2; ++part) {  // 0: low nibbles, 1: high nibbles
 #pragma unroll
@@ -147,18 +170,17 @@ __device__ __forceinline__ void dequant_half(uint32_t bp, int g, uint32_t taddr)
           if constexpr (kQ4Codes<QT>) {
             if (part == 0) {
               // 0.5 + q/256, q in 0..15:  w = f*(256 d sc) - (128 d sc + dmin m)
-              four_weights(q & 0x0F0F0F0Fu, 2, 256.0f * dsl, -(128.0f * dsl + dml), col[2 * w], col[2 * w + 1]);
+              four_weights(q & 0x0F0F0F0Fu, 2, Al, dml, exl, col[2 * w], col[2 * w + 1]);
             } else {
               // 16q in byte position 1: f = 0.5 + 16q/65536 = 0.5 + q/4096
-              four_weights(q & 0xF0F0F0F0u, 1, 4096.0f * dsh, -(2048.0f * dsh + dmh), col[2 * w], col[2 * w + 1]);
+              four_weights(q & 0xF0F0F0F0u, 1, Ah, dmh, exh, col[2 * w], col[2 * w + 1]);
             }
           } else {
             const uint32_t hb = (w < 4) ? w4(qh0, w) : w4(qh1, w - 4);
             uint32_t v;
             if (part == 0) v = (q & 0x0F0F0F0Fu) | (((hb >> (2 * c)) & 0x01010101u) << 4);
             else v = ((q >> 4) & 0x0F0F0F0Fu) | (((hb >> (2 * c + 1)) & 0x01010101u) << 4);
-            const float A = part ? dsh : dsl, M0 = part ? dmh : dml;
-            four_weights(v, 2, 256.0f * A, -(128.0f * A + M0), col[2 * w], col[2 * w + 1]);
+            four_weights(v, 2, part ? Ah : Al, part ? dmh : dml, part ? exh : exl, col[2 * w], col[2 * w + 1]);
           }
         }
         tmem_st16(taddr + 32 * cc + 16 * part, col);
@@ -187,8 +209,8 @@ __device__ __forceinline__ void dequant_half(uint32_t bp, int g, uint32_t taddr)
         else if (p == 2) v = ((a >> 4) & 0x0F0F0F0Fu) | (hv & 0x30303030u);
         else v = ((b >> 4) & 0x0F0F0F0Fu) | ((hv >> 2) & 0x30303030u);
         const float A = ds[2 * p + (w >> 2)];
-        // 0.5 + q/256, q in 0..63:  w = f*(256 d sc) - 160 d sc  ( = d sc (q - 32) )
-        four_weights(v, 2, 256.0f * A, -160.0f * A, col[2 * (w & 7)], col[2 * (w & 7) + 1]);
+        // 0.5 + q/256, q in 0..63:  w = f*(256 d sc) - 160 d sc  ( = d sc (q - 32); 160 d sc is exact)
+        four_weights(v, 2, 256.0f * A, 32.0f * A, true, col[2 * (w & 7)], col[2 * (w & 7) + 1]);
       }
       tmem_st16(taddr + 16 * p, col);
     }

@@ -143,6 +143,21 @@ kq_status kq_dequant_bf16(int type, const void *blocks, uint16_t *out, int64_t n
  * memory (exact integer dots per block; each row then equals that token's
  * M = 1 product bit for bit); otherwise M = 2..16 with bf16 x on the tensor
  * cores (weights rounded to bf16); M >= 2 with fp32 x on the CUDA cores.
+ * Accuracy, for finite x and weights and partial sums in fp32's normal range:
+ * |y - y_exact| <= e * sum_k |w[n][k] x[m][k]|, where
+ *   - M = 1, and M = 2..4 with bf16 x: x is held exactly in shared memory (a
+ *     24-bit integer image per 128 values, plus the values off its grid, each
+ *     applied on its own; fp32 x as two bf16 parts, dropping <= 2^-18 |x|)
+ *     and each lane's 64-weight block contribution is formed from exact
+ *     integers (rounded once where its d and dmin terms can cancel, at most
+ *     five times where they cannot): e <= 2^-24 (D + 6) (+ 2^-18 with fp32 x),
+ *     D the fp32 additions from a term to y: ceil(K/256) + 21, plus one per
+ *     value off the grid in the lane's blocks;
+ *   - tensor cores (bf16 x): each weight rounded once to fp32, then to bf16:
+ *     e <= 2^-8 + 2^-24 (ceil(K/16) + 8), taking each 16-term MMA step as one
+ *     rounding into the fp32 accumulator;
+ *   - M >= 2 with fp32 x: each weight rounded once to fp32, fp32 FMAs:
+ *     e <= 2^-24 (2 ceil(K/256) + 16).
  */
 kq_status kq_matvec(int type, const void *W, const void *x, int x_dtype, float *y, int64_t N, int64_t K,
                     int64_t M, kq_stream_t stream);
@@ -258,9 +273,11 @@ kq_status kq_moe_matvec(int type, const void *W_experts, int32_t n_experts, cons
  *   - It allocates nothing.  The first call on each device looks up the
  *     array's address once (cudaGetSymbolAddress); make that first call
  *     before any stream capture begins.
- *   - The array is zero when the library loads and is left with its arrival
- *     counters at zero after every call; a routed id out of range is reported
- *     in the library's device error word (kq_device_error), not in a workspace.
+ *   - The array keeps what the last call left, laid out for that call's
+ *     shape; a call with gate_w first clears its own arrival counters (a
+ *     stream-ordered cudaMemsetAsync on the array, which allocates nothing).
+ *     A routed id out of range is reported in the library's device error
+ *     word (kq_device_error), not in a workspace.
  *   - Calls that overlap in time (on any stream or host thread) share the
  *     array and race: issue them one after another.
  */
