@@ -161,7 +161,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -191,7 +191,7 @@ class ClockSampler:
                 if len(r) > 3 + i and r[3 + i].lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "interval_ms": 20}
 
 
 def cpu_baseline(mats_host, seconds=12.0):
@@ -324,6 +324,124 @@ def _timed_graph(torch, fn, stream, steps, warmup):
     e1.record(stream)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / steps
+
+
+def dev_matrix(torch, synth, qt, N, K, gen):
+    """N x ceil(K/256) blocks generated on the device by the input recipe of
+    synth.gen_blocks (uniform code, scale and min bytes; d, dmin =
+    fp16(|N(0, 0.002)|); Q6_K scales over the full int8 range), flattened to
+    bytes.  For the large benchmark weight sets, which would take minutes to
+    draw on the host; a different random stream from the host generator."""
+    nbl = N * synth.n_blocks_per_row(K)
+    raw = torch.randint(0, 256, (nbl, synth.BLOCK_BYTES[qt]), dtype=torch.uint8, device="cuda", generator=gen)
+
+    def half_bytes():
+        h = (torch.randn(nbl, device="cuda", generator=gen) * 0.002).abs().half()
+        return h.view(torch.uint8).view(nbl, 2)
+    if qt in (synth.Q4_K, synth.Q5_K):
+        raw[:, 0:2] = half_bytes()
+        raw[:, 2:4] = half_bytes()
+    elif qt == synth.Q6_K:
+        raw[:, 208:210] = half_bytes()
+    else:
+        raise ValueError("device generation covers the k-quant formats")
+    return raw.view(-1)
+
+
+def graph_ms(torch, fn, stream, steps, warmup):
+    return _timed_graph(torch, fn, stream, steps, warmup)
+
+
+def dense_case(torch, kq, synth, qt, N, K, M, xd, seed, steps, warmup, stream, span=320 << 20, min_copies=1):
+    """One product repeated over enough distinct weight copies that every
+    replay reads HBM; returns (weight bytes, ms per product)."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    W0 = dev_matrix(torch, synth, qt, N, K, gen)
+    ncopy = max(min_copies, -(-span // W0.numel()))
+    Ws = [W0] + [W0.clone() for _ in range(ncopy - 1)]
+    x = torch.randn((M, K), device="cuda", generator=gen)
+    x = x.to(torch.bfloat16) if xd == "bf16" else x
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    xdt = kq.KQ_BF16 if xd == "bf16" else kq.KQ_F32
+
+    def step():
+        for W in Ws:
+            kq.kq_matvec(qt, W, x, xdt, y, N, K, M, stream)
+    ms = graph_ms(torch, step, stream, steps, warmup) / ncopy
+    del Ws
+    return synth.matrix_bytes(qt, N, K), ms
+
+
+def moe_case(torch, kq, synth, M, steps, warmup, stream, rho=0.0, layers=30, seed=2):
+    """The routed-MoE decode step of the MoE workload: 30 layers of router +
+    expert FFN (128 experts, top-8, gate/up 2816->704, down 704->2816) + a
+    shared FFN 2816->2112->2816, Q4_K, bf16 x; weights generated on the
+    device.  Returns the step's ms, stored bytes read (distinct routed experts
+    + shared FFN) and the experts per layer."""
+    qt, E, H, F, SH, top_k = synth.Q4_K, 128, 2816, 704, 2112, 8
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    per = []
+    for li in range(layers):
+        L = {"Wg": dev_matrix(torch, synth, qt, E * F, H, gen), "Wu": dev_matrix(torch, synth, qt, E * F, H, gen),
+             "Wd": dev_matrix(torch, synth, qt, E * H, F, gen), "Sg": dev_matrix(torch, synth, qt, SH, H, gen),
+             "Su": dev_matrix(torch, synth, qt, SH, H, gen), "Sd": dev_matrix(torch, synth, qt, H, SH, gen)}
+        z = torch.randn((M, E), device="cuda", generator=gen)
+        if rho:  # a per-layer component shared by the tokens of the block (correlated routing)
+            z = (rho ** 0.5) * torch.randn((1, E), device="cuda", generator=gen) + ((1 - rho) ** 0.5) * z
+        L["logits"] = z.contiguous()
+        L["ids"] = torch.empty((M, top_k), dtype=torch.int32, device="cuda")
+        L["gate"] = torch.empty((M, top_k), dtype=torch.float32, device="cuda")
+        L["ffn"] = kq.ffn_weights(qt, qt, E, kq.KQ_ACT_GELU_TANH, F, L["Wg"], L["Wu"], L["Wd"], SH, L["Sg"],
+                                  L["Su"], L["Sd"])
+        per.append(L)
+    x = torch.randn((M, H), device="cuda", generator=gen).to(torch.bfloat16)
+    y = torch.empty((M, H), dtype=torch.float32, device="cuda")
+    ws = kq.moe_ffn_workspace(H, F, SH, M, top_k, E)
+
+    def step():
+        for L in per:
+            kq.kq_moe_route(L["logits"], M, E, top_k, L["ids"], L["gate"], None, stream)
+            kq.kq_moe_ffn(L["ffn"], L["ids"], L["gate"], x, kq.KQ_BF16, y, H, M, top_k, ws, ws.numel(), stream)
+    ms = graph_ms(torch, step, stream, steps, warmup)
+    kq.kq_moe_check(ws)
+    eb = synth.matrix_bytes(qt, F, H) * 2 + synth.matrix_bytes(qt, H, F)
+    sb = synth.matrix_bytes(qt, SH, H) * 2 + synth.matrix_bytes(qt, H, SH)
+    nexp = [int(torch.unique(L["ids"]).numel()) for L in per]
+    nbytes = sum(n * eb + sb for n in nexp)
+    del per
+    torch.cuda.empty_cache()
+    return ms, nbytes, sum(nexp) / layers
+
+
+def other_configs(torch, kq, synth, stream, steps, warmup, peak):
+    """The benchmark's other configurations, measured in the same run after
+    the headline: ms per step and GB/s of stored weight bytes each."""
+    out = {}
+
+    def rec(b, ms, **kw):
+        r = {"ms": round(ms, 5), "GB/s": round(b / (ms * 1e-3) / 1e9, 1), "frac_of_hbm_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4)}
+        r.update(kw)
+        return r
+    b, ms = dense_case(torch, kq, synth, synth.Q4_K, 4096, 4096, 1, "f32", 0, steps, warmup, stream, span=0,
+                       min_copies=64)
+    out["single_q4k_4096x4096_f32x"] = rec(b, ms)
+    sweep = {}
+    for qt, nm in ((synth.Q4_K, "Q4_K"), (synth.Q5_K, "Q5_K"), (synth.Q6_K, "Q6_K")):
+        for M in (1, 2, 4, 8):
+            b, ms = dense_case(torch, kq, synth, qt, 4096, 14336, M, "bf16", 1, steps, warmup, stream)
+            sweep[f"{nm}/M={M}"] = rec(b, ms)
+    out["format_sweep_4096x14336_bf16x"] = sweep
+    tb, tms = 0, 0.0
+    for N, K in ((14336, 4096), (14336, 4096), (4096, 14336)):
+        b, ms = dense_case(torch, kq, synth, synth.Q4_K, N, K, 16, "bf16", 3, steps, warmup, stream)
+        tb, tms = tb + b, tms + ms
+    out["verify_block_m16_gate_up_down"] = rec(tb, tms, tok_s_equiv=round(16e3 / tms, 1))
+    for M in (1, 16):
+        ms, b, ne = moe_case(torch, kq, synth, M, min(steps, 10), warmup, stream)
+        out[f"moe_30_layers_m{M}"] = rec(b, ms, tok_s_equiv=round(M * 1e3 / ms, 1), experts_per_layer=round(ne, 1))
+    return out
 
 
 def run_workload(args):
@@ -520,6 +638,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kq", choices=["kq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other configurations in the JSON line")
     ap.add_argument("--single", default=None,
                     help="profiling helper: run one product TYPE:NxK[:M[:f32|bf16]] (e.g. Q4_K:19456x2560), or one MoE layer moe_ffn:TYPE:M, --steps times")
     ap.add_argument("--workload", default=None, choices=["q4k_4096", "format_sweep", "verify16", "moe", "dequant"],
@@ -669,6 +788,11 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(host_sample(synth, n_mats=7))
+    configs = None
+    if not args.no_configs:
+        del graphs, step_graph, chain, stage_runs
+        torch.cuda.empty_cache()
+        configs = other_configs(torch, kq, synth, stream, min(args.steps, 20), args.warmup, load_peaks()[0])
 
     if rank == 0:
         gbs = job_gbs(total_bytes, world, ms)
@@ -694,8 +818,12 @@ def main():
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "gpu_launches": launches[best] * args.steps,
                 "clocks": clk.summary(), "device": device_info(torch)}
+        if line["clocks"]["sm_mhz"]:  # the step in SM clock cycles at the median clock of the timed region
+            line["clocks"]["mcycles_per_step"] = round(ms * line["clocks"]["sm_mhz"] * 1e-3, 4)
         if cpu is not None:
             line["cpu_baseline"] = cpu
+        if configs is not None:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

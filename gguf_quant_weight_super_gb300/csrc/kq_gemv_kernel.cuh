@@ -69,6 +69,10 @@ constexpr int NTH = NTHC + 32;         // + one producer warp
 constexpr int RING_MAX = 8;                // ring slots at most
 constexpr int CONSUMER_BAR = 1;        // named barrier of the consumer warps
 constexpr int MAX_NB = 64;             // K <= 16384
+// Shared memory header: full and empty mbarriers (RING_MAX each) and the
+// reduction counters (RING_MAX + 1).
+constexpr int kHdrBytes = 512;
+static_assert(16 * RING_MAX + 4 * (RING_MAX + 1) <= kHdrBytes, "header");
 constexpr int kMaxTokens1 = 4;         // tokens of one single-product launch (bf16 x when more than one)
 // Largest stage (32 row segments): 48 KB keeps a ring of at least 4 slots.
 constexpr int64_t kSlotCap = 48 * 1024;
@@ -233,12 +237,14 @@ __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, 
           const int bl = 2 * gi + (c >> 1);  // this lane's block within the stage
           if (bl < n) {
             const int b = b0 + bl;
+            // the hi image of fp32 x is combined exactly; bf16 images and the lo
+            // image (2^-9 of the value) take the checked fp32 combine
             if constexpr (SUM) {  // hi and lo images of one x: one copy of the code, two passes
 #pragma unroll 1
-              for (int t = 0; t < NI; ++t) block_half<QT, R>(t ? xs[NI - 1] : xs[0], b, c & 1, rp, acc[0]);
+              for (int t = 0; t < NI; ++t) block_half<QT, R>(t ? xs[NI - 1] : xs[0], b, c & 1, rp, t != 0, acc[0]);
             } else {
 #pragma unroll
-              for (int t = 0; t < NI; ++t) block_half<QT, R>(xs[t], b, c & 1, rp, acc[t]);
+              for (int t = 0; t < NI; ++t) block_half<QT, R>(xs[t], b, c & 1, rp, true, acc[t]);
             }
           }
 #pragma unroll
@@ -311,14 +317,20 @@ __device__ __forceinline__ void fixup_op(const KqOp& o, int cta, int G, int ctid
 
 // A program op: bf16 x (one image) or fp32 x (hi and lo images), any format
 // (XK0: the program's x dtypes, 1 = bf16 only, 2 = fp32 only, 0 = both).
+// Programs take tiles of 32 rows.
+template <int QT, int XK0>
+__device__ __forceinline__ void consume_bf16(const KqOp& o, const XImg (&x1)[1], const Ring& rg, const Red& rd,
+                                             Walk& wk, int* err, int cta, int G) {
+  consume_op<QT, 4, 1, false>(o, x1, rg, rd, wk, err, cta, G);
+}
 template <int XK0>
 __device__ __forceinline__ void consume_any(const KqOp& o, bool bf16, const XImg (&xs)[2], const Ring& rg,
                                             const Red& rd, Walk& wk, int* err, int cta, int G) {
   const XImg x1[1] = {xs[0]};
   if (XK0 == 1 || (XK0 == 0 && bf16)) {
-    if (o.type == T_Q4_K) consume_op<T_Q4_K, 4, 1, false>(o, x1, rg, rd, wk, err, cta, G);
-    else if (o.type == T_Q5_K) consume_op<T_Q5_K, 4, 1, false>(o, x1, rg, rd, wk, err, cta, G);
-    else consume_op<T_Q6_K, 4, 1, false>(o, x1, rg, rd, wk, err, cta, G);
+    if (o.type == T_Q4_K) consume_bf16<T_Q4_K, XK0>(o, x1, rg, rd, wk, err, cta, G);
+    else if (o.type == T_Q5_K) consume_bf16<T_Q5_K, XK0>(o, x1, rg, rd, wk, err, cta, G);
+    else consume_bf16<T_Q6_K, XK0>(o, x1, rg, rd, wk, err, cta, G);
   } else {
     if (o.type == T_Q4_K) consume_op<T_Q4_K, 4, 2, true>(o, xs, rg, rd, wk, err, cta, G);
     else if (o.type == T_Q5_K) consume_op<T_Q5_K, 4, 2, true>(o, xs, rg, rd, wk, err, cta, G);
@@ -383,7 +395,7 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
   Ring rg;
   rg.full = reinterpret_cast<uint64_t*>(smem);
   rg.empty = rg.full + RING_MAX;
-  rg.base = smem + 256;
+  rg.base = smem + kHdrBytes;
   rg.base_s = smem_u32(rg.base);
   rg.S = a.S;
   rg.slot = a.slot;
@@ -624,7 +636,7 @@ struct LaunchGeom {
 // nimg x images of nb_max blocks; mt outputs per row (reduction buffers)
 bool ring_geom(int64_t max_stage, int nb_max, int nimg, LaunchGeom& g, int mt = 1) {
   g.slot = static_cast<int>((max_stage + 127) & ~int64_t(127));
-  const size_t fixed = 256 + nimg * ximg_stride(nb_max);
+  const size_t fixed = kHdrBytes + nimg * ximg_stride(nb_max);
   int S = RING_MAX;
   while (S >= 2 && fixed + static_cast<size_t>(S) * g.slot + red_bytes(S, mt) > static_cast<size_t>(kMaxSmemPerBlock))
     --S;

@@ -219,8 +219,8 @@ __device__ __forceinline__ void put_oct(const float (&v)[8], int o, const XImg& 
   float mx = 0.0f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(v[j]));
-#pragma unroll
-  for (int w = 1; w < 32; w <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, w));
+  // block maximum: non-negative floats order as their bit patterns
+  mx = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mx)));
   // shift = 22 - e, mx = f * 2^e, f in [0.5, 1): from the bits for normal values
   const int be = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu);
   const int shift = (be >= 40 && be <= 200) ? 148 - be : run_shift_slow(mx);
@@ -417,10 +417,11 @@ __device__ __forceinline__ float combine45(float d, float dmin, const Acc45& A) 
 }
 
 // Q4_K / Q5_K / IA4: adds chunk c of the block at bp (16-byte aligned) to A;
-// si = the chunk's two 32-run sums of m.
+// si = the chunk's two 32-run sums of m; sc0, sc1, m0, m1 its sub-blocks'
+// scales and mins (1 for IA4).
 template <int QT>
-__device__ __forceinline__ void chunk45(uint32_t bp, const XSlice& X, int2 si, int c, const ScaleLane& sl, Acc45& A) {
-  const uint4 hdr = lds128(bp);
+__device__ __forceinline__ void chunk45(uint32_t bp, const XSlice& X, int2 si, int c, int sc0, int sc1, int m0,
+                                        int m1, Acc45& A) {
   constexpr int QS = kQ4Codes<QT> ? 16 : 48;
   const uint4 q0 = lds128(bp + QS + 32 * c);
   const uint4 q1 = lds128(bp + QS + 32 * c + 16);
@@ -455,24 +456,48 @@ __device__ __forceinline__ void chunk45(uint32_t bp, const XSlice& X, int2 si, i
 #pragma unroll
     for (int l = 0; l < NLB; ++l) I[1][l] >>= 4;  // exact: every term is a multiple of 16
   }
-  int sc0 = 1, sc1 = 1, m0 = 1, m1 = 1;
-  if constexpr (QT != T_IA4) {  // IA4: the chunk is one group, sc = m = 1
-    const uint32_t P = __byte_perm(sl.lowsrc ? hdr.y : hdr.w, hdr.z, sl.selP);
-    const uint32_t Q = __byte_perm(hdr.y, hdr.z, sl.selQ);
-    const uint32_t L = (P & sl.mA) | ((P >> 4) & sl.mB) | ((Q >> 2) & sl.mH);
-    sc0 = static_cast<int>(L & 0xFF);
-    sc1 = static_cast<int>((L >> 8) & 0xFF);
-    m0 = static_cast<int>((L >> 16) & 0xFF);
-    m1 = static_cast<int>(L >> 24);
-  }
   A.Y0 += sc0 * I[0][0] + sc1 * I[1][0];
   A.Y1 += sc0 * I[0][1] + sc1 * I[1][1];
   A.Y2 += sc0 * I[0][2] + sc1 * I[1][2];
   A.Mi += static_cast<long long>(m0) * si.x + static_cast<long long>(m1) * si.y;
 }
-// acc + s (d Y - dmin Mi): one block's (Q4_K/Q5_K) or one group's (IA4, group c) sums.
+// Scales and mins of chunk c's sub-blocks (2c, 2c+1) from the block header
+// (quad layout: the per-lane constants of scale_lane).
+__device__ __forceinline__ void chunk_scales(const uint4& hdr, const ScaleLane& sl, int& sc0, int& sc1, int& m0,
+                                             int& m1) {
+  const uint32_t P = __byte_perm(sl.lowsrc ? hdr.y : hdr.w, hdr.z, sl.selP);
+  const uint32_t Q = __byte_perm(hdr.y, hdr.z, sl.selQ);
+  const uint32_t L = (P & sl.mA) | ((P >> 4) & sl.mB) | ((Q >> 2) & sl.mH);
+  sc0 = static_cast<int>(L & 0xFF);
+  sc1 = static_cast<int>((L >> 8) & 0xFF);
+  m0 = static_cast<int>((L >> 16) & 0xFF);
+  m1 = static_cast<int>(L >> 24);
+}
+// Scale bytes (sc of sub-blocks 4h..4h+3) and min bytes of half h of a block.
+__device__ __forceinline__ void half_scales(const uint4& hdr, int h, uint32_t& scb, uint32_t& mb) {
+  scb = h ? ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u)) : (hdr.y & 0x3F3F3F3Fu);
+  mb = h ? (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u)) : (hdr.z & 0x3F3F3F3Fu);
+}
+
+// d Y - dmin Mi for images whose tolerance leaves room (bf16 x, the lo part
+// of fp32 x): in fp32 when that is provably within 2^-11 of the result, else
+// exactly (combine45).  The fp32 form's error is at most 3u bnd + u |v| (the
+// int-to-float conversions and the two-step limb sum take at most 3u of
+// bnd = |d| (|Y0| 2^16 + |Y1| 2^8 + |Y2|) + |dmin Mi|); it is kept when
+// bnd <= 2^11 |v|, i.e. within 3 2^-13 |v| + u |v| < 2^-11 |v|.
+__device__ __forceinline__ float combine45_checked(float d, float dmin, const Acc45& A) {
+  const float y0 = __int2float_rn(A.Y0), y1 = __int2float_rn(A.Y1), y2 = __int2float_rn(A.Y2);
+  const float yf = __fmaf_rn(y0, 65536.0f, __fmaf_rn(y1, 256.0f, y2));
+  const float yb = __fmaf_rn(fabsf(y0), 65536.0f, __fmaf_rn(fabsf(y1), 256.0f, fabsf(y2)));
+  const float mt = dmin * __ll2float_rn(A.Mi);
+  const float v = __fmaf_rn(d, yf, -mt);
+  if (__fmaf_rn(fabsf(d), yb, fabsf(mt)) <= 2048.0f * fabsf(v)) return v;
+  return combine45(d, dmin, A);
+}
+// acc + s (d Y - dmin Mi): one block's (Q4_K/Q5_K) or one group's (IA4, group
+// c) sums; exactly rounded, or (checked) within 2^-11 of it.
 template <int QT>
-__device__ __forceinline__ float finish45(uint32_t bp, const Acc45& A, float s, int c, float acc) {
+__device__ __forceinline__ float finish45(uint32_t bp, const Acc45& A, float s, int c, bool checked, float acc) {
   const uint4 hdr = lds128(bp);
   float d, dmin;
   if constexpr (QT == T_IA4) {
@@ -482,7 +507,7 @@ __device__ __forceinline__ float finish45(uint32_t bp, const Acc45& A, float s, 
     d = half_bits_to_float(hdr.x & 0xFFFF);
     dmin = half_bits_to_float(hdr.x >> 16);
   }
-  return __fmaf_rn(s, combine45(d, dmin, A), acc);
+  return __fmaf_rn(s, checked ? combine45_checked(d, dmin, A) : combine45(d, dmin, A), acc);
 }
 
 // Q6_K: adds chunk c of the block at bp (2-byte aligned) to A; si = the
@@ -532,10 +557,12 @@ __device__ __forceinline__ float finish6(uint32_t bp, const Acc6& A, float s, fl
 // One chunk c of the block at bp, combined on its own (quad layout).
 template <int QT>
 __device__ __forceinline__ float core_q45(uint32_t bp, const XSlice& X, int2 si, float s, int c, const ScaleLane& sl,
-                                          float acc) {
+                                          bool checked, float acc) {
   Acc45 A = {0, 0, 0, 0};
-  chunk45<QT>(bp, X, si, c, sl, A);
-  return finish45<QT>(bp, A, s, c, acc);
+  int sc0 = 1, sc1 = 1, m0 = 1, m1 = 1;
+  if constexpr (QT != T_IA4) chunk_scales(lds128(bp), sl, sc0, sc1, m0, m1);  // IA4: one group, sc = m = 1
+  chunk45<QT>(bp, X, si, c, sc0, sc1, m0, m1, A);
+  return finish45<QT>(bp, A, s, c, checked, acc);
 }
 __device__ __forceinline__ float core_q6(uint32_t bp, const XSlice& X, int4 si, float s, int c, float acc) {
   Acc6 A = {0, 0, 0, 0};
@@ -600,7 +627,7 @@ __device__ __noinline__ float block_extra(uint32_t bp, const XImg xi, int b, uin
 // values it leaves out (every fourth one).
 template <int QT, int R>
 __device__ __forceinline__ void block_rows(const XImg& xi, int b, const uint32_t (&rp)[R], int c, const ScaleLane& sl,
-                                           float (&acc)[R]) {
+                                           bool checked, float (&acc)[R]) {
   const uint4 bh = lds128(hdr_s(xi, b));
   const float s = __uint_as_float(bh.x);
   const uint32_t cnt = bh.z;
@@ -617,7 +644,7 @@ __device__ __forceinline__ void block_rows(const XImg& xi, int b, const uint32_t
       const uint2 sv = lds64(si32_s(xi, b, c));
       const int2 si = make_int2(static_cast<int>(sv.x), static_cast<int>(sv.y));
 #pragma unroll
-      for (int i = 0; i < R; ++i) acc[i] = core_q45<QT>(rp[i], X, si, s, c, sl, acc[i]);
+      for (int i = 0; i < R; ++i) acc[i] = core_q45<QT>(rp[i], X, si, s, c, sl, checked, acc[i]);
     }
   }
   if (cnt != 0) {
@@ -631,7 +658,8 @@ __device__ __forceinline__ void block_rows(const XImg& xi, int b, const uint32_t
 // the half, combined once per row (IA4: once per group), then every second
 // value the image leaves out.
 template <int QT, int R>
-__device__ __forceinline__ void block_half(const XImg& xi, int b, int h, const uint32_t (&rp)[R], float (&acc)[R]) {
+__device__ __forceinline__ void block_half(const XImg& xi, int b, int h, const uint32_t (&rp)[R], bool checked,
+                                           float (&acc)[R]) {
   const uint4 bh = lds128(hdr_s(xi, b));
   const float s = __uint_as_float(bh.x);
   const uint32_t cnt = bh.z;
@@ -656,8 +684,12 @@ __device__ __forceinline__ void block_half(const XImg& xi, int b, int h, const u
       for (int i = 0; i < R; ++i) acc[i] = finish6(rp[i], A[i], s, acc[i]);
     } else {
       Acc45 A[R];
+      uint32_t scb[R], mb[R];  // the half's scale and min bytes, per row
 #pragma unroll
-      for (int i = 0; i < R; ++i) A[i] = Acc45{0, 0, 0, 0};
+      for (int i = 0; i < R; ++i) {
+        A[i] = Acc45{0, 0, 0, 0};
+        if constexpr (QT != T_IA4) half_scales(lds128(rp[i]), h, scb[i], mb[i]);
+      }
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int c = 2 * h + k;
@@ -665,19 +697,24 @@ __device__ __forceinline__ void block_half(const XImg& xi, int b, int h, const u
         load_slice<QT>(xl + 4 * slice_off<QT>(c), 4 * xi.plane, X);
         const uint2 sv = lds64(si32_s(xi, b, c));
         const int2 si = make_int2(static_cast<int>(sv.x), static_cast<int>(sv.y));
-        const ScaleLane sl = scale_lane(c);
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-          chunk45<QT>(rp[i], X, si, c, sl, A[i]);
-          if constexpr (QT == T_IA4) {  // each group has its own scale and bias
-            acc[i] = finish45<QT>(rp[i], A[i], s, c, acc[i]);
+          if constexpr (QT == T_IA4) {  // each group has its own scale and bias (sc = m = 1)
+            chunk45<QT>(rp[i], X, si, c, 1, 1, 1, 1, A[i]);
+            acc[i] = finish45<QT>(rp[i], A[i], s, c, checked, acc[i]);
             A[i] = Acc45{0, 0, 0, 0};
+          } else {
+            const int sc0 = static_cast<int>((scb[i] >> (16 * k)) & 0xFFu);
+            const int sc1 = static_cast<int>((scb[i] >> (16 * k + 8)) & 0xFFu);
+            const int m0 = static_cast<int>((mb[i] >> (16 * k)) & 0xFFu);
+            const int m1 = static_cast<int>((mb[i] >> (16 * k + 8)) & 0xFFu);
+            chunk45<QT>(rp[i], X, si, c, sc0, sc1, m0, m1, A[i]);
           }
         }
       }
       if constexpr (QT != T_IA4) {
 #pragma unroll
-        for (int i = 0; i < R; ++i) acc[i] = finish45<QT>(rp[i], A[i], s, 0, acc[i]);
+        for (int i = 0; i < R; ++i) acc[i] = finish45<QT>(rp[i], A[i], s, 0, checked, acc[i]);
       }
     }
   }

@@ -53,9 +53,11 @@ SIGNATURES = {
 
 
 # The sources each kernel family is compiled from (the one-token / program
-# kernel: kq_gemv.cu and the headers it includes).
+# kernel: kq_gemv_kernel.cuh, the translation units that instantiate it and
+# the headers it includes).
 KERNEL_SOURCES = {
-    "prog_kernel": ("kq_gemv.cu", "kq_lane.cuh", "kq_ptx.cuh", "kq_internal.h", "kq_decode.cuh"),
+    "prog_kernel": ("kq_gemv_kernel.cuh", "kq_gemv.cu", "kq_gemv_q4k.cu", "kq_gemv_q5k.cu", "kq_gemv_q6k.cu",
+                    "kq_gemv_ia4.cu", "kq_lane.cuh", "kq_ptx.cuh", "kq_internal.h", "kq_decode.cuh"),
 }
 
 
