@@ -268,6 +268,8 @@ def run_single(args):
     spec = args.single.split(":")
     if spec[0] == "moe_ffn":  # moe_ffn:<type>:<M>: one MoE layer's router + expert FFN (128 experts top-8)
         return run_single_ffn(args, spec)
+    if spec[0] == "dequant":  # dequant:<type>:<N>x<K>:<fp32|bf16>: expansion of a whole matrix
+        return run_single_dequant(args, spec)
     qt = {"Q4_K": synth.Q4_K, "Q5_K": synth.Q5_K, "Q6_K": synth.Q6_K, "IA4": synth.IA4}[spec[0]]
     N, K = (int(v) for v in spec[1].split("x"))
     M = int(spec[2]) if len(spec) > 2 else 1
@@ -279,6 +281,22 @@ def run_single(args):
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
     for _ in range(args.steps):
         kq.kq_matvec(qt, W, x, kq.KQ_BF16 if xd == "bf16" else kq.KQ_F32, y, N, K, M)
+    torch.cuda.synchronize()
+    assert kq.kq_device_error() == 0
+    print(json.dumps({"single": args.single, "runs": args.steps, "ok": True}))
+
+
+def run_single_dequant(args, spec):
+    """Dequantize one N x K matrix to fp32 or bf16, `--steps` times."""
+    import torch
+    from gguf_quant_weight_super_gb300 import kq, synth
+    qt = {"Q4_K": synth.Q4_K, "Q5_K": synth.Q5_K, "Q6_K": synth.Q6_K, "IA4": synth.IA4}[spec[1]]
+    N, K = (int(v) for v in spec[2].split("x"))
+    W = torch.from_numpy(synth.gen_matrix(qt, N, K, synth.rng(0, qt, N, K))).cuda()
+    bf = len(spec) > 3 and spec[3] == "bf16"
+    out = torch.empty(N * K, dtype=torch.bfloat16 if bf else torch.float32, device="cuda")
+    for _ in range(args.steps):
+        (kq.kq_dequant_bf16 if bf else kq.kq_dequant)(qt, W, out, N * K)
     torch.cuda.synchronize()
     assert kq.kq_device_error() == 0
     print(json.dumps({"single": args.single, "runs": args.steps, "ok": True}))
@@ -640,7 +658,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other configurations in the JSON line")
     ap.add_argument("--single", default=None,
-                    help="profiling helper: run one product TYPE:NxK[:M[:f32|bf16]] (e.g. Q4_K:19456x2560), or one MoE layer moe_ffn:TYPE:M, --steps times")
+                    help="profiling helper: run one product TYPE:NxK[:M[:f32|bf16]] (e.g. Q4_K:19456x2560), one MoE layer moe_ffn:TYPE:M, or one expansion dequant:TYPE:NxK:fp32|bf16, --steps times")
     ap.add_argument("--workload", default=None, choices=["q4k_4096", "format_sweep", "verify16", "moe", "dequant"],
                     help="time another configuration instead of the dense sweep (one JSON line each)")
     args = ap.parse_args()
