@@ -237,14 +237,15 @@ __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, 
           const int bl = 2 * gi + (c >> 1);  // this lane's block within the stage
           if (bl < n) {
             const int b = b0 + bl;
-            // the hi image of fp32 x is combined exactly; bf16 images and the lo
-            // image (2^-9 of the value) take the checked fp32 combine
+            // the hi image of fp32 x takes the tighter fp32 combine check
+            // (kLimHi), bf16 images and the lo image (2^-9 of the value) kLimBf16
             if constexpr (SUM) {  // hi and lo images of one x: one copy of the code, two passes
 #pragma unroll 1
-              for (int t = 0; t < NI; ++t) block_half<QT, R>(t ? xs[NI - 1] : xs[0], b, c & 1, rp, t != 0, acc[0]);
+              for (int t = 0; t < NI; ++t)
+                block_half<QT, R>(t ? xs[NI - 1] : xs[0], b, c & 1, rp, t ? kLimBf16 : kLimHi, acc[0]);
             } else {
 #pragma unroll
-              for (int t = 0; t < NI; ++t) block_half<QT, R>(xs[t], b, c & 1, rp, true, acc[t]);
+              for (int t = 0; t < NI; ++t) block_half<QT, R>(xs[t], b, c & 1, rp, kLimBf16, acc[t]);
             }
           }
 #pragma unroll

@@ -110,6 +110,24 @@ __device__ __forceinline__ float mul_pow2(float f, int e) {
   return (f * __uint_as_float(static_cast<uint32_t>(127 + e1) << 23)) *
          __uint_as_float(static_cast<uint32_t>(127 + e - e1) << 23);
 }
+// v rounded to the nearest fp32 (ties to even), in single-precision and
+// integer operations only: |v| below 2^48 is split into two parts of 24 bits,
+// each converted exactly, and one fma rounds their sum once; a larger |v|
+// first drops its low 16 bits into a sticky bit (the result keeps at least 32
+// significant bits, so the one rounding is unchanged) and is scaled back by
+// 2^16 exactly.
+__device__ __forceinline__ float ll2f_rn(long long v) {
+  const unsigned long long a = v < 0 ? 0ull - static_cast<unsigned long long>(v) : static_cast<unsigned long long>(v);
+  unsigned long long b = a;
+  float scale = 1.0f;
+  if (a >= (1ull << 48)) {
+    b = (a >> 16) | ((a & 0xFFFFull) != 0 ? 1ull : 0ull);
+    scale = 65536.0f;
+  }
+  const float r = __fmaf_rn(__uint2float_rn(static_cast<uint32_t>(b >> 24)), 16777216.0f,
+                            __uint2float_rn(static_cast<uint32_t>(b & 0xFFFFFFull))) * scale;
+  return v < 0 ? -r : r;
+}
 // 2^e as a float for e in [-149, 127] (subnormal below -126)
 __device__ __forceinline__ float pow2f(int e) {
   return e >= -126 ? __uint_as_float(static_cast<uint32_t>(127 + e) << 23) : __uint_as_float(1u << (e + 149));
@@ -394,7 +412,7 @@ struct Acc6 {
 // (exponents far apart, zero, subnormal or non-finite: out of line, rare)
 static __device__ __noinline__ float combine45_far(float d, float dmin, int Y0, int Y1, int Y2, long long Mi) {
   const long long Y = (static_cast<long long>(Y0) << 16) + (static_cast<long long>(Y1) << 8) + Y2;
-  return __fmaf_rn(d, __ll2float_rn(Y), -dmin * __ll2float_rn(Mi));
+  return __fmaf_rn(d, ll2f_rn(Y), -dmin * ll2f_rn(Mi));
 }
 __device__ __forceinline__ float combine45(float d, float dmin, const Acc45& A) {
   const uint32_t ud = __float_as_uint(d), um = __float_as_uint(dmin);
@@ -411,7 +429,7 @@ __device__ __forceinline__ float combine45(float d, float dmin, const Acc45& A) 
     P = P * 256 + static_cast<long long>(alpha) * A.Y1;
     P = P * 256 + static_cast<long long>(alpha) * A.Y2;
     P -= static_cast<long long>(beta) * A.Mi;
-    return mul_pow2(__ll2float_rn(P), min(ed, em) - 137);  // unit 2^(min exponent - 127 - 10)
+    return mul_pow2(ll2f_rn(P), min(ed, em) - 137);  // unit 2^(min exponent - 127 - 10)
   }
   return combine45_far(d, dmin, A.Y0, A.Y1, A.Y2, A.Mi);
 }
@@ -479,25 +497,30 @@ __device__ __forceinline__ void half_scales(const uint4& hdr, int h, uint32_t& s
   mb = h ? (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u)) : (hdr.z & 0x3F3F3F3Fu);
 }
 
-// d Y - dmin Mi for images whose tolerance leaves room (bf16 x, the lo part
-// of fp32 x): in fp32 when that is provably within 2^-11 of the result, else
-// exactly (combine45).  The fp32 form's error is at most 3u bnd + u |v| (the
-// int-to-float conversions and the two-step limb sum take at most 3u of
-// bnd = |d| (|Y0| 2^16 + |Y1| 2^8 + |Y2|) + |dmin Mi|); it is kept when
-// bnd <= 2^11 |v|, i.e. within 3 2^-13 |v| + u |v| < 2^-11 |v|.
-__device__ __forceinline__ float combine45_checked(float d, float dmin, const Acc45& A) {
+// d Y - dmin Mi in fp32 when that is provably within (3 lim + 1) u of the
+// result (u = 2^-24), else exactly (combine45).  The fp32 form's error is at
+// most 3u bnd + u |v| (the int-to-float conversions and the two-step limb sum
+// take at most 3u of bnd = |d| (|Y0| 2^16 + |Y1| 2^8 + |Y2|) + |dmin Mi|); it
+// is kept when bnd <= lim |v|:
+//   kLimBf16 = 2^11 (bf16 x, and the lo image of fp32 x): < 2^-11 |v|;
+//   kLimHi = 2^8 (the hi image of fp32 x): < 769 u |v| < 4.6e-5 |v|.
+// |v| is at most the sum of |w m| over the weights summed, so these are
+// bounds relative to sum |w x|.
+constexpr float kLimBf16 = 2048.0f;
+constexpr float kLimHi = 256.0f;
+__device__ __forceinline__ float combine45_checked(float d, float dmin, const Acc45& A, float lim) {
   const float y0 = __int2float_rn(A.Y0), y1 = __int2float_rn(A.Y1), y2 = __int2float_rn(A.Y2);
   const float yf = __fmaf_rn(y0, 65536.0f, __fmaf_rn(y1, 256.0f, y2));
   const float yb = __fmaf_rn(fabsf(y0), 65536.0f, __fmaf_rn(fabsf(y1), 256.0f, fabsf(y2)));
-  const float mt = dmin * __ll2float_rn(A.Mi);
+  const float mt = dmin * ll2f_rn(A.Mi);
   const float v = __fmaf_rn(d, yf, -mt);
-  if (__fmaf_rn(fabsf(d), yb, fabsf(mt)) <= 2048.0f * fabsf(v)) return v;
+  if (__fmaf_rn(fabsf(d), yb, fabsf(mt)) <= lim * fabsf(v)) return v;
   return combine45(d, dmin, A);
 }
 // acc + s (d Y - dmin Mi): one block's (Q4_K/Q5_K) or one group's (IA4, group
-// c) sums; exactly rounded, or (checked) within 2^-11 of it.
+// c) sums, in fp32 within the bound lim gives (combine45_checked).
 template <int QT>
-__device__ __forceinline__ float finish45(uint32_t bp, const Acc45& A, float s, int c, bool checked, float acc) {
+__device__ __forceinline__ float finish45(uint32_t bp, const Acc45& A, float s, int c, float lim, float acc) {
   const uint4 hdr = lds128(bp);
   float d, dmin;
   if constexpr (QT == T_IA4) {
@@ -507,7 +530,7 @@ __device__ __forceinline__ float finish45(uint32_t bp, const Acc45& A, float s, 
     d = half_bits_to_float(hdr.x & 0xFFFF);
     dmin = half_bits_to_float(hdr.x >> 16);
   }
-  return __fmaf_rn(s, checked ? combine45_checked(d, dmin, A) : combine45(d, dmin, A), acc);
+  return __fmaf_rn(s, combine45_checked(d, dmin, A, lim), acc);
 }
 
 // Q6_K: adds chunk c of the block at bp (2-byte aligned) to A; si = the
@@ -551,18 +574,18 @@ __device__ __forceinline__ void chunk6(uint32_t bp, const XSlice& X, int4 si, in
 __device__ __forceinline__ float finish6(uint32_t bp, const Acc6& A, float s, float acc) {
   const float d = half_bits_to_float(lds16(bp + 208));
   const long long Y = (static_cast<long long>(A.Y0) << 16) + (static_cast<long long>(A.Y1) << 8) + A.Y2 - 32 * A.Z;
-  return __fmaf_rn(s * d, __ll2float_rn(Y), acc);
+  return __fmaf_rn(s * d, ll2f_rn(Y), acc);
 }
 
 // One chunk c of the block at bp, combined on its own (quad layout).
 template <int QT>
 __device__ __forceinline__ float core_q45(uint32_t bp, const XSlice& X, int2 si, float s, int c, const ScaleLane& sl,
-                                          bool checked, float acc) {
+                                          float lim, float acc) {
   Acc45 A = {0, 0, 0, 0};
   int sc0 = 1, sc1 = 1, m0 = 1, m1 = 1;
   if constexpr (QT != T_IA4) chunk_scales(lds128(bp), sl, sc0, sc1, m0, m1);  // IA4: one group, sc = m = 1
   chunk45<QT>(bp, X, si, c, sc0, sc1, m0, m1, A);
-  return finish45<QT>(bp, A, s, c, checked, acc);
+  return finish45<QT>(bp, A, s, c, lim, acc);
 }
 __device__ __forceinline__ float core_q6(uint32_t bp, const XSlice& X, int4 si, float s, int c, float acc) {
   Acc6 A = {0, 0, 0, 0};
@@ -571,9 +594,10 @@ __device__ __forceinline__ float core_q6(uint32_t bp, const XSlice& X, int4 si, 
 }
 
 // Weight k of the block at bp as the exactly rounded fp32 value (the
-// definition's d*sc*q - dmin*m, d*sc*(q-32) or scale*q + bias, one rounding).
+// definition's d*sc*q - dmin*m, d*sc*(q-32) or scale*q + bias, one rounding);
+// hdr = the block's first 16 bytes (Q4_K, Q5_K, IA4; Q6_K reads its own d).
 template <int QT>
-__device__ __forceinline__ float w_at(uint32_t bp, int k) {
+__device__ __forceinline__ float w_at_h(uint32_t bp, int k, const uint4& hdr) {
   if constexpr (QT == T_Q6_K) {
     const int h = k >> 7, r = k & 127, t = r >> 5, l = r & 31;
     const uint32_t qlb = lds8(bp + 64 * h + 32 * (t & 1) + l);
@@ -587,7 +611,6 @@ __device__ __forceinline__ float w_at(uint32_t bp, int k) {
     const uint32_t cb = lds8(bp + QS + 32 * (k >> 6) + (k & 31));
     int q = static_cast<int>((cb >> (4 * ((k >> 5) & 1))) & 15u);
     if constexpr (QT == T_Q5_K) q |= static_cast<int>((lds8(bp + 16 + (k & 31)) >> (k >> 5)) & 1u) << 4;
-    const uint4 hdr = lds128(bp);
     if constexpr (QT == T_IA4) {
       const int g = k >> 6;
       return __fmaf_rn(ia4_scale(hdr, g), static_cast<float>(q), -ia4_neg_bias(hdr, g));
@@ -601,33 +624,126 @@ __device__ __forceinline__ float w_at(uint32_t bp, int k) {
   }
 }
 
-// The values of block b that the integer image leaves out, for the row whose
-// block is at bp: listed values (cnt <= ECAP), or every value of a raw block;
-// this lane takes values first, first + step, ...  acc += fl(w_k x_k) for each.
-template <int QT>
-__device__ __noinline__ float block_extra(uint32_t bp, const XImg xi, int b, uint32_t cnt, int first, int step,
-                                          float acc) {
-  if (cnt <= static_cast<uint32_t>(ECAP)) {
-    for (int j = first; j < static_cast<int>(cnt); j += step) {
-      const uint32_t e = xi.limb[ent_word(xi, b, j)];
-      acc = __fmaf_rn(w_at<QT>(bp, static_cast<int>(e & 0xFFu)), __uint_as_float(e & 0xFFFF0000u), acc);
-    }
-  } else {
-    for (int k = first; k < 256; k += step) {
-      const uint32_t wv = xi.limb[raw_word(xi, b, k)];
-      const float xv = __uint_as_float((k & 1) ? (wv & 0xFFFF0000u) : (wv << 16));
-      if (xv != 0.0f) acc = __fmaf_rn(w_at<QT>(bp, k), xv, acc);
-    }
+// The listed values of block b (cnt <= ECAP) for the R rows whose blocks are
+// at rp: this lane takes entries first, first + step, ...; each entry's word
+// is read once for all the rows, each row's header once for all entries.
+// acc[i] += fl(w_k x_k) for each (the same per-value arithmetic as below).
+template <int QT, int R>
+__device__ __forceinline__ void entries_rows(const XImg& xi, int b, int cnt, int first, int step,
+                                             const uint32_t (&rp)[R], float (&acc)[R]) {
+  uint4 hd[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) hd[i] = QT == T_Q6_K ? make_uint4(0, 0, 0, 0) : lds128(rp[i]);
+#pragma unroll 1
+  for (int j = first; j < cnt; j += step) {
+    const uint32_t e = lds32(xi.limb_s + 4 * ent_word(xi, b, j));
+    const int k = static_cast<int>(e & 0xFFu);
+    const float xv = __uint_as_float(e & 0xFFFF0000u);
+#pragma unroll
+    for (int i = 0; i < R; ++i) acc[i] = __fmaf_rn(w_at_h<QT>(rp[i], k, hd[i]), xv, acc[i]);
   }
-  return acc;
 }
+
+// A raw block (all 256 values kept as bf16): chunk cc of block b for the R
+// rows at rp, acc[i] += fl(w_k x_k) over the chunk's 64 weights in order,
+// with w_k the exactly rounded fp32 weight of w_at.  The chunk's x values are
+// read once for all the rows; each code byte is decoded once per row.
+__device__ __forceinline__ float nib_f(uint32_t w, int s) {  // (w >> s) & 15 as a float, exactly
+  return __uint_as_float(0x4B000000u | ((w >> s) & 15u)) - 8388608.0f;
+}
+template <int QT, int R>
+__device__ __forceinline__ void raw_rows(const XImg& xi, int b, int cc, const uint32_t (&rp)[R], float (&acc)[R]) {
+  // x of the chunk's weights, in the order the codes come: Q4_K/Q5_K/IA4 lo
+  // nibbles 64cc + i, hi nibbles 64cc + 32 + i (i < 32); Q6_K part p, value i:
+  // weight 128 (cc >> 1) + 32 p + 16 (cc & 1) + i (i < 16)
+  uint32_t xw[32];  // bf16 pairs (even value low)
+#pragma unroll
+  for (int q4 = 0; q4 < 16; ++q4) {
+    const int k = (QT == T_Q6_K) ? 128 * (cc >> 1) + 32 * (q4 >> 2) + 16 * (cc & 1) + 4 * (q4 & 3)
+                                 : 64 * cc + 32 * (q4 >> 3) + 4 * (q4 & 7);
+    const uint2 v = lds64(xi.limb_s + 4 * raw_word(xi, b, k));
+    xw[2 * q4] = v.x;
+    xw[2 * q4 + 1] = v.y;
+  }
+  auto xv = [&](int idx) {  // x of the idx-th weight of the chunk (in code order)
+    const uint32_t w = xw[idx >> 1];
+    return __uint_as_float((idx & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  };
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const uint32_t bp = rp[i];
+    float a = acc[i];
+    if constexpr (QT == T_Q6_K) {
+      const int h = cc >> 1, e = cc & 1;
+      const uint4 qa = lds16_a2(bp + 64 * h + 16 * e);
+      const uint4 qb = lds16_a2(bp + 64 * h + 32 + 16 * e);
+      const uint4 qh = lds16_a2(bp + 128 + 32 * h + 16 * e);
+      const uint2 sv = lds8_a2(bp + 192 + 8 * h);
+      const uint32_t se = __byte_perm(sv.x, sv.y, e ? 0x7531 : 0x6420);  // scales 8h + 2p + e
+      const float d = half_bits_to_float(lds16(bp + 208));
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int sc = sbyte(se, p);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t av = w4(qa, w), bv = w4(qb, w), hv = w4(qh, w);
+          const uint32_t cd = p == 0 ? ((av & 0x0F0F0F0Fu) | ((hv << 4) & 0x30303030u))
+                            : p == 1 ? ((bv & 0x0F0F0F0Fu) | ((hv << 2) & 0x30303030u))
+                            : p == 2 ? (((av >> 4) & 0x0F0F0F0Fu) | (hv & 0x30303030u))
+                                     : (((bv >> 4) & 0x0F0F0F0Fu) | ((hv >> 2) & 0x30303030u));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int q = static_cast<int>((cd >> (8 * j)) & 0xFFu);
+            a = __fmaf_rn(d * static_cast<float>(sc * (q - 32)), xv(16 * p + 4 * w + j), a);
+          }
+        }
+      }
+    } else {
+      constexpr int QS = kQ4Codes<QT> ? 16 : 48;
+      const uint4 q0 = lds128(bp + QS + 32 * cc), q1 = lds128(bp + QS + 32 * cc + 16);
+      uint4 h0 = make_uint4(0, 0, 0, 0), h1 = make_uint4(0, 0, 0, 0);
+      if constexpr (QT == T_Q5_K) { h0 = lds128(bp + 16); h1 = lds128(bp + 32); }
+      const uint4 hdr = lds128(bp);
+      float A0, B0, A1, B1;  // lo nibbles: sub-block 2cc (IA4: group cc), hi: 2cc + 1
+      if constexpr (QT == T_IA4) {
+        A0 = A1 = ia4_scale(hdr, cc);
+        B0 = B1 = ia4_neg_bias(hdr, cc);
+      } else {
+        const uint32_t bs = scale_min_bytes(hdr.y, hdr.z, hdr.w, cc);  // [sc_2g, sc_2g+1, m_2g, m_2g+1]
+        const float d = half_bits_to_float(hdr.x & 0xFFFF), dmin = half_bits_to_float(hdr.x >> 16);
+        A0 = d * static_cast<float>(bs & 0xFFu);
+        A1 = d * static_cast<float>((bs >> 8) & 0xFFu);
+        B0 = dmin * static_cast<float>((bs >> 16) & 0xFFu);
+        B1 = dmin * static_cast<float>(bs >> 24);
+      }
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const uint32_t q = (w < 4) ? w4(q0, w) : w4(q1, w - 4);
+        uint32_t hb = 0;
+        if constexpr (QT == T_Q5_K) hb = (w < 4) ? w4(h0, w) : w4(h1, w - 4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float qlo = nib_f(q, 8 * j), qhi = nib_f(q, 8 * j + 4);
+          if constexpr (QT == T_Q5_K) {
+            qlo += static_cast<float>(((hb >> (8 * j + 2 * cc)) & 1u) << 4);
+            qhi += static_cast<float>(((hb >> (8 * j + 2 * cc + 1)) & 1u) << 4);
+          }
+          a = __fmaf_rn(__fmaf_rn(A0, qlo, -B0), xv(4 * w + j), a);
+          a = __fmaf_rn(__fmaf_rn(A1, qhi, -B1), xv(32 + 4 * w + j), a);
+        }
+      }
+    }
+    acc[i] = a;
+  }
+}
+
 
 // Quad layout: one image's contribution of block b to the rows at rp[0..R)
 // (R rows per quad), lane c taking chunk c: the integer image, then the
 // values it leaves out (every fourth one).
 template <int QT, int R>
 __device__ __forceinline__ void block_rows(const XImg& xi, int b, const uint32_t (&rp)[R], int c, const ScaleLane& sl,
-                                           bool checked, float (&acc)[R]) {
+                                           float lim, float (&acc)[R]) {
   const uint4 bh = lds128(hdr_s(xi, b));
   const float s = __uint_as_float(bh.x);
   const uint32_t cnt = bh.z;
@@ -644,12 +760,13 @@ __device__ __forceinline__ void block_rows(const XImg& xi, int b, const uint32_t
       const uint2 sv = lds64(si32_s(xi, b, c));
       const int2 si = make_int2(static_cast<int>(sv.x), static_cast<int>(sv.y));
 #pragma unroll
-      for (int i = 0; i < R; ++i) acc[i] = core_q45<QT>(rp[i], X, si, s, c, sl, checked, acc[i]);
+      for (int i = 0; i < R; ++i) acc[i] = core_q45<QT>(rp[i], X, si, s, c, sl, lim, acc[i]);
     }
   }
-  if (cnt != 0) {
-#pragma unroll
-    for (int i = 0; i < R; ++i) acc[i] = block_extra<QT>(rp[i], xi, b, cnt, c, 4, acc[i]);
+  if (cnt > static_cast<uint32_t>(ECAP)) {
+    raw_rows<QT, R>(xi, b, c, rp, acc);
+  } else if (cnt != 0) {
+    entries_rows<QT, R>(xi, b, static_cast<int>(cnt), c, 4, rp, acc);
   }
 }
 
@@ -658,7 +775,7 @@ __device__ __forceinline__ void block_rows(const XImg& xi, int b, const uint32_t
 // the half, combined once per row (IA4: once per group), then every second
 // value the image leaves out.
 template <int QT, int R>
-__device__ __forceinline__ void block_half(const XImg& xi, int b, int h, const uint32_t (&rp)[R], bool checked,
+__device__ __forceinline__ void block_half(const XImg& xi, int b, int h, const uint32_t (&rp)[R], float lim,
                                            float (&acc)[R]) {
   const uint4 bh = lds128(hdr_s(xi, b));
   const float s = __uint_as_float(bh.x);
@@ -701,7 +818,7 @@ __device__ __forceinline__ void block_half(const XImg& xi, int b, int h, const u
         for (int i = 0; i < R; ++i) {
           if constexpr (QT == T_IA4) {  // each group has its own scale and bias (sc = m = 1)
             chunk45<QT>(rp[i], X, si, c, 1, 1, 1, 1, A[i]);
-            acc[i] = finish45<QT>(rp[i], A[i], s, c, checked, acc[i]);
+            acc[i] = finish45<QT>(rp[i], A[i], s, c, lim, acc[i]);
             A[i] = Acc45{0, 0, 0, 0};
           } else {
             const int sc0 = static_cast<int>((scb[i] >> (16 * k)) & 0xFFu);
@@ -714,13 +831,15 @@ __device__ __forceinline__ void block_half(const XImg& xi, int b, int h, const u
       }
       if constexpr (QT != T_IA4) {
 #pragma unroll
-        for (int i = 0; i < R; ++i) acc[i] = finish45<QT>(rp[i], A[i], s, 0, checked, acc[i]);
+        for (int i = 0; i < R; ++i) acc[i] = finish45<QT>(rp[i], A[i], s, 0, lim, acc[i]);
       }
     }
   }
-  if (cnt != 0) {
-#pragma unroll
-    for (int i = 0; i < R; ++i) acc[i] = block_extra<QT>(rp[i], xi, b, cnt, h, 2, acc[i]);
+  if (cnt > static_cast<uint32_t>(ECAP)) {
+    raw_rows<QT, R>(xi, b, 2 * h, rp, acc);
+    raw_rows<QT, R>(xi, b, 2 * h + 1, rp, acc);
+  } else if (cnt != 0) {
+    entries_rows<QT, R>(xi, b, static_cast<int>(cnt), h, 2, rp, acc);
   }
 }
 

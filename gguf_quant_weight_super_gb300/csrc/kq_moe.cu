@@ -104,7 +104,7 @@ __device__ __forceinline__ void pair_rows(uint32_t rp, uint32_t rstride, int nb,
 #pragma unroll
     for (int i = 0; i < RQ; ++i) rb[i] = rp + i * rstride + b * BB;
 #pragma unroll
-    for (int t = 0; t < NI; ++t) block_rows<QT, RQ>(xs[t], b, rb, c, sl, NI == 1 || t != 0, a);
+    for (int t = 0; t < NI; ++t) block_rows<QT, RQ>(xs[t], b, rb, c, sl, (NI == 1 || t != 0) ? kLimBf16 : kLimHi, a);
   }
 #pragma unroll
   for (int i = 0; i < RQ; ++i) {
