@@ -134,7 +134,15 @@ bool plan_prog(const ProgOpDesc* descs, int n_ops, KqOp* ops, size_t* part_bytes
     o.K = static_cast<int32_t>(descs[i].K);
     o.type = descs[i].type;
     o.x_bf16 = descs[i].x_bf16;
-    if (!plan_op(o, G, any_wait && split_allowed(descs, n_ops, i), kSlotCap)) return false;
+    const bool split = any_wait && split_allowed(descs, n_ops, i);
+    if (!plan_op(o, G, split, kSlotCap)) return false;
+    // a bf16 Q6_K op whose 32-row whole-row stage exceeds the other ops'
+    // largest (the 4B sweep's LM head, 67 KB) would set the chain's slot size
+    // and leave two slots: 16-row tiles keep it at 34 KB
+    if (o.type == T_Q6_K && o.x_bf16 && o.contig && stage_bytes(o) > kSlotCap) {
+      KqOp o2 = o;
+      if (plan_op(o2, G, split, kSlotCap, false, 2) && o2.contig) o = o2;
+    }
     ops[i] = o;
   }
   if (any_wait)

@@ -322,6 +322,9 @@ __device__ __forceinline__ void fixup_op(const KqOp& o, int cta, int G, int ctid
 template <int QT, int XK0>
 __device__ __forceinline__ void consume_bf16(const KqOp& o, const XImg (&x1)[1], const Ring& rg, const Red& rd,
                                              Walk& wk, int* err, int cta, int G) {
+  if constexpr (QT == T_Q6_K) {  // Q6_K ops whose 32-row stage would not fit the chain's slots take 16 rows
+    if (o.R == 2) { consume_op<QT, 2, 1, false>(o, x1, rg, rd, wk, err, cta, G); return; }
+  }
   consume_op<QT, 4, 1, false>(o, x1, rg, rd, wk, err, cta, G);
 }
 template <int XK0>
@@ -585,7 +588,7 @@ void set_split(KqOp& o, int KS, int kcmax) {
 // Geometry of one op: K-parts KS (only with a workspace) and stage width KC.
 // cost = block-chunks of the busiest CTA (a chunk = one block for 32 rows,
 // dealt to one warp), plus a fixed cost per stage and per split.
-bool plan_op(KqOp& o, int G, bool allow_split, int64_t slot_cap, bool allow_short_tiles = false) {
+bool plan_op(KqOp& o, int G, bool allow_split, int64_t slot_cap, bool allow_short_tiles = false, int force_R = 0) {
   const int BB = block_bytes_of(o.type);
   if (!BB || o.K <= 0 || o.K % 32 || o.N <= 0) return false;
   o.nb = (o.K + 255) / 256;
@@ -607,6 +610,7 @@ bool plan_op(KqOp& o, int G, bool allow_split, int64_t slot_cap, bool allow_shor
       if (best < 0 || cost < best - 1e-9) { best = cost; o.R = r; }
     }
   }
+  if (force_R) o.R = force_R;
   const int TTo = 8 * o.R;
   const int64_t ntiles = (o.N + TTo - 1) / TTo;
   if (ntiles > (int64_t(1) << 28)) return false;

@@ -625,34 +625,70 @@ __device__ __forceinline__ float w_at_h(uint32_t bp, int k, const uint4& hdr) {
 }
 
 // The listed values of block b (cnt <= ECAP) for the R rows whose blocks are
-// at rp: this lane takes entries first, first + step, ...; each entry's word
-// is read once for all the rows, each row's header once for all entries.
-// acc[i] += fl(w_k x_k) for each (the same per-value arithmetic as below).
+// at rp: this lane takes entries first, first + step, ... (at most 16); each
+// entry's word is read once for all the rows, each row's header once for all
+// entries.  acc[i] += the sum of fl(w_k x_k) over them, w_k the exactly
+// rounded weight, summed on its own first (at most 17 fp32 additions from a
+// product to acc).
+// R row addresses / R row sums passed by value (the rare paths below are out
+// of line, so that the integer core keeps its registers).
+template <int R>
+struct RowAddr {
+  uint32_t v[R];
+};
+template <int R>
+struct RowSum {
+  float v[R];
+};
 template <int QT, int R>
-__device__ __forceinline__ void entries_rows(const XImg& xi, int b, int cnt, int first, int step,
-                                             const uint32_t (&rp)[R], float (&acc)[R]) {
+__device__ __noinline__ RowSum<R> entries_rows_ol(const XImg xi, int b, int cnt, int first, int step,
+                                                  const RowAddr<R> rp_, RowSum<R> acc_) {
+  const uint32_t (&rp)[R] = rp_.v;
+  float (&acc)[R] = acc_.v;
   uint4 hd[R];
+  float t[R];
 #pragma unroll
-  for (int i = 0; i < R; ++i) hd[i] = QT == T_Q6_K ? make_uint4(0, 0, 0, 0) : lds128(rp[i]);
+  for (int i = 0; i < R; ++i) {
+    hd[i] = QT == T_Q6_K ? make_uint4(0, 0, 0, 0) : lds128(rp[i]);
+    t[i] = 0.0f;
+  }
 #pragma unroll 1
   for (int j = first; j < cnt; j += step) {
     const uint32_t e = lds32(xi.limb_s + 4 * ent_word(xi, b, j));
     const int k = static_cast<int>(e & 0xFFu);
     const float xv = __uint_as_float(e & 0xFFFF0000u);
 #pragma unroll
-    for (int i = 0; i < R; ++i) acc[i] = __fmaf_rn(w_at_h<QT>(rp[i], k, hd[i]), xv, acc[i]);
+    for (int i = 0; i < R; ++i) t[i] = __fmaf_rn(w_at_h<QT>(rp[i], k, hd[i]), xv, t[i]);
   }
+#pragma unroll
+  for (int i = 0; i < R; ++i) acc[i] = __fadd_rn(acc[i], t[i]);
+  return acc_;
+}
+template <int QT, int R>
+__device__ __forceinline__ void entries_rows(const XImg& xi, int b, int cnt, int first, int step,
+                                             const uint32_t (&rp)[R], float (&acc)[R]) {
+  RowAddr<R> ra;
+  RowSum<R> rs;
+#pragma unroll
+  for (int i = 0; i < R; ++i) { ra.v[i] = rp[i]; rs.v[i] = acc[i]; }
+  rs = entries_rows_ol<QT, R>(xi, b, cnt, first, step, ra, rs);
+#pragma unroll
+  for (int i = 0; i < R; ++i) acc[i] = rs.v[i];
 }
 
 // A raw block (all 256 values kept as bf16): chunk cc of block b for the R
-// rows at rp, acc[i] += fl(w_k x_k) over the chunk's 64 weights in order,
-// with w_k the exactly rounded fp32 weight of w_at.  The chunk's x values are
-// read once for all the rows; each code byte is decoded once per row.
+// rows at rp: acc[i] += the sum of fl(w_k x_k) over the chunk's 64 weights,
+// w_k the exactly rounded fp32 weight of w_at_h, summed as four running sums
+// of 16 products, added pairwise (at most 19 fp32 additions from a product
+// to acc).  The chunk's x values are read once for all the rows; each code
+// byte is decoded once per row.
 __device__ __forceinline__ float nib_f(uint32_t w, int s) {  // (w >> s) & 15 as a float, exactly
   return __uint_as_float(0x4B000000u | ((w >> s) & 15u)) - 8388608.0f;
 }
 template <int QT, int R>
-__device__ __forceinline__ void raw_rows(const XImg& xi, int b, int cc, const uint32_t (&rp)[R], float (&acc)[R]) {
+__device__ __noinline__ RowSum<R> raw_rows_ol(const XImg xi, int b, int cc, const RowAddr<R> rp_, RowSum<R> acc_) {
+  const uint32_t (&rp)[R] = rp_.v;
+  float (&acc)[R] = acc_.v;
   // x of the chunk's weights, in the order the codes come: Q4_K/Q5_K/IA4 lo
   // nibbles 64cc + i, hi nibbles 64cc + 32 + i (i < 32); Q6_K part p, value i:
   // weight 128 (cc >> 1) + 32 p + 16 (cc & 1) + i (i < 16)
@@ -672,7 +708,7 @@ __device__ __forceinline__ void raw_rows(const XImg& xi, int b, int cc, const ui
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const uint32_t bp = rp[i];
-    float a = acc[i];
+    float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if constexpr (QT == T_Q6_K) {
       const int h = cc >> 1, e = cc & 1;
       const uint4 qa = lds16_a2(bp + 64 * h + 16 * e);
@@ -694,7 +730,7 @@ __device__ __forceinline__ void raw_rows(const XImg& xi, int b, int cc, const ui
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int q = static_cast<int>((cd >> (8 * j)) & 0xFFu);
-            a = __fmaf_rn(d * static_cast<float>(sc * (q - 32)), xv(16 * p + 4 * w + j), a);
+            a[j] = __fmaf_rn(d * static_cast<float>(sc * (q - 32)), xv(16 * p + 4 * w + j), a[j]);
           }
         }
       }
@@ -728,13 +764,24 @@ __device__ __forceinline__ void raw_rows(const XImg& xi, int b, int cc, const ui
             qlo += static_cast<float>(((hb >> (8 * j + 2 * cc)) & 1u) << 4);
             qhi += static_cast<float>(((hb >> (8 * j + 2 * cc + 1)) & 1u) << 4);
           }
-          a = __fmaf_rn(__fmaf_rn(A0, qlo, -B0), xv(4 * w + j), a);
-          a = __fmaf_rn(__fmaf_rn(A1, qhi, -B1), xv(32 + 4 * w + j), a);
+          a[j] = __fmaf_rn(__fmaf_rn(A0, qlo, -B0), xv(4 * w + j), a[j]);
+          a[j] = __fmaf_rn(__fmaf_rn(A1, qhi, -B1), xv(32 + 4 * w + j), a[j]);
         }
       }
     }
-    acc[i] = a;
+    acc[i] = __fadd_rn(acc[i], __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])));
   }
+  return acc_;
+}
+template <int QT, int R>
+__device__ __forceinline__ void raw_rows(const XImg& xi, int b, int cc, const uint32_t (&rp)[R], float (&acc)[R]) {
+  RowAddr<R> ra;
+  RowSum<R> rs;
+#pragma unroll
+  for (int i = 0; i < R; ++i) { ra.v[i] = rp[i]; rs.v[i] = acc[i]; }
+  rs = raw_rows_ol<QT, R>(xi, b, cc, ra, rs);
+#pragma unroll
+  for (int i = 0; i < R; ++i) acc[i] = rs.v[i];
 }
 
 

@@ -145,14 +145,19 @@ kq_status kq_dequant_bf16(int type, const void *blocks, uint16_t *out, int64_t n
  * cores (weights rounded to bf16); M >= 2 with fp32 x on the CUDA cores.
  * Accuracy, for finite x and weights and partial sums in fp32's normal range:
  * |y - y_exact| <= e * sum_k |w[n][k] x[m][k]|, where
- *   - M = 1, and M = 2..4 with bf16 x: x is held exactly in shared memory (a
- *     24-bit integer image per 128 values, plus the values off its grid, each
- *     applied on its own; fp32 x as two bf16 parts, dropping <= 2^-18 |x|)
- *     and each lane's 64-weight block contribution is formed from exact
- *     integers (rounded once where its d and dmin terms can cancel, at most
- *     five times where they cannot): e <= 2^-24 (D + 6) (+ 2^-18 with fp32 x),
- *     D the fp32 additions from a term to y: ceil(K/256) + 21, plus one per
- *     value off the grid in the lane's blocks;
+ *   - M = 1, and M = 2..4 with bf16 x: x is held exactly in shared memory (per
+ *     256 values a 24-bit integer image with a power-of-two scale; the values
+ *     off its grid listed beside it, or, past 32 of them, the whole block kept
+ *     as bf16; fp32 x as two bf16 parts hi and lo, dropping <= 2^-18 |x|).
+ *     Each lane's 128-weight half-block sum d*Y - dmin*Mi is formed from
+ *     exact integers and rounded to fp32 where that is provably within a
+ *     bound of the exact value, else exactly (one rounding): within 2^-11 for
+ *     bf16 x and for the lo part, within 4.6e-5 for the hi part of fp32 x.
+ *     Listed and kept values add fl(w x), w the exactly rounded weight.
+ *     bf16 x:  e <= 2^-11 + 2^-24 D;
+ *     fp32 x:  e <= 4.6e-5 + 2^-19 + 2^-18 + 2^-24 D (below 1e-4: this path
+ *     takes K <= 16384), D = 3 ceil(K/256) + 40 bounding the fp32 additions
+ *     from a term to y;
  *   - tensor cores (bf16 x): each weight rounded once to fp32, then to bf16:
  *     e <= 2^-8 + 2^-24 (ceil(K/16) + 8), taking each 16-term MMA step as one
  *     rounding into the fp32 accumulator;
@@ -239,6 +244,9 @@ kq_status kq_chain_run(const kq_chain_plan *plan, void *workspace, kq_stream_t s
  * The (token, slot) pairs are grouped by expert on the device, and every
  * distinct routed expert's rows are read from memory once per call.  Sums
  * are fp32 in a fixed order (the gate-weighted sum adds slots in order).
+ * Accuracy: each pair's product takes kq_matvec's M = 1 arithmetic (the same
+ * exact x image and per-lane combine), so each y[m][j] (or each gated term
+ * g y) is within kq_matvec's M = 1 bound with D increased by 2 + top_k.
  * An id outside [0, n_experts) never faults: its pair is dropped (no
  * contribution; without gate_w its output row is not written) and the
  * workspace's error word is set (kq_moe_check).
