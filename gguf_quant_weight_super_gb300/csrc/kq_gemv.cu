@@ -157,6 +157,38 @@ bool plan_prog(const ProgOpDesc* descs, int n_ops, KqOp* ops, size_t* part_bytes
   *part_bytes = pb;
   return true;
 }
+
+// Ops that start an x (the first op, or one that waits or reads a new x).
+bool starts_x(const ProgOpDesc* descs, int i) {
+  return i == 0 || descs[i].wait_previous || descs[i].x != descs[i - 1].x || descs[i].K != descs[i - 1].K ||
+         descs[i].x_bf16 != descs[i - 1].x_bf16;
+}
+size_t xrange_bytes(const ProgOpDesc* descs, int n_ops, int G) {
+  size_t n = 0;
+  for (int i = 0; i < n_ops; ++i) n += starts_x(descs, i) ? 1 : 0;
+  return align256(n * G * sizeof(int32_t));
+}
+// Blocks of x that CTA cta reads in ops [i, j) (all sharing one x): the
+// union of its units' K-parts (one K-part per op when the grid is a multiple
+// of the op's K-parts, every unit of a CTA then having the same one).
+int32_t cta_xrange(const KqOp* ops, int i, int j, int cta, int G) {
+  int lo = 1 << 15, hi = 0;
+  for (int k = i; k < j; ++k) {
+    const KqOp& o = ops[k];
+    const int u = first_unit(o, cta, G);
+    if (u >= o.nunits) continue;
+    int a = 0, b = o.nb;
+    if (o.KS > 1 && G % o.KS == 0) {
+      const int kp = u % o.KS;
+      a = kp * o.kpb;
+      b = std::min(o.nb, a + o.kpb);
+    }
+    lo = std::min(lo, a);
+    hi = std::max(hi, b);
+  }
+  if (hi <= lo) lo = hi = 0;  // no unit: nothing to stage
+  return lo | (hi << 16);
+}
 }  // namespace
 
 size_t prog_workspace_size(const ProgOpDesc* descs, int n_ops) {
@@ -165,7 +197,9 @@ size_t prog_workspace_size(const ProgOpDesc* descs, int n_ops) {
   size_t pb = 0;
   const bool ok = plan_prog(descs, n_ops, ops, &pb);
   delete[] ops;
-  return ok ? align256(kHeaderBytes + static_cast<size_t>(n_ops) * sizeof(KqOp)) + pb : 0;
+  return ok ? align256(kHeaderBytes + static_cast<size_t>(n_ops) * sizeof(KqOp)) + pb +
+                  xrange_bytes(descs, n_ops, num_sms())
+            : 0;
 }
 
 cudaError_t prog_prepare(const ProgOpDesc* descs, int n_ops, void* ws, size_t ws_bytes, ProgPlan* plan,
@@ -175,7 +209,8 @@ cudaError_t prog_prepare(const ProgOpDesc* descs, int n_ops, void* ws, size_t ws
   KqOp* ops = new KqOp[n_ops];
   size_t pb = 0;
   if (!plan_prog(descs, n_ops, ops, &pb)) { delete[] ops; return cudaErrorNotSupported; }
-  const size_t need = align256(kHeaderBytes + static_cast<size_t>(n_ops) * sizeof(KqOp)) + pb;
+  const size_t need =
+      align256(kHeaderBytes + static_cast<size_t>(n_ops) * sizeof(KqOp)) + pb + xrange_bytes(descs, n_ops, G);
   if (ws_bytes < need) { delete[] ops; return cudaErrorInvalidValue; }
   uint8_t* w = static_cast<uint8_t*>(ws);
   size_t off = align256(kHeaderBytes + static_cast<size_t>(n_ops) * sizeof(KqOp));
@@ -201,6 +236,16 @@ cudaError_t prog_prepare(const ProgOpDesc* descs, int n_ops, void* ws, size_t ws
   }
   for (int i = last_wait; i < n_ops; ++i)
     if (ops[i].KS > 1) final_fix = 1;  // not summed at any later grid barrier
+  // per x: the blocks each CTA stages (after the partial sums)
+  std::vector<int32_t> xr;
+  for (int i = 0; i < n_ops;) {
+    int j = i + 1;
+    while (j < n_ops && !starts_x(descs, j)) ++j;
+    ops[i].xrange = reinterpret_cast<const int32_t*>(w + off) + xr.size();
+    for (int c = 0; c < G; ++c) xr.push_back(cta_xrange(ops, i, j, c, G));
+    for (int k = i + 1; k < j; ++k) ops[k].xrange = nullptr;
+    i = j;
+  }
   LaunchGeom g;
   const int nimg = any_f32 ? 2 : 1;  // fp32 x takes two images (hi, lo)
   if (!ring_geom(max_stage, nb_max, nimg, g)) { delete[] ops; return cudaErrorNotSupported; }
@@ -218,6 +263,8 @@ cudaError_t prog_prepare(const ProgOpDesc* descs, int n_ops, void* ws, size_t ws
   cudaError_t e = cudaMemsetAsync(ws, 0, kHeaderBytes, stream);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(w + kHeaderBytes, ops, sizeof(KqOp) * n_ops, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(w + off, xr.data(), sizeof(int32_t) * xr.size(), cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   delete[] ops;
   return e;

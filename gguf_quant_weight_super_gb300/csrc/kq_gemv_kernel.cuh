@@ -98,6 +98,10 @@ struct KqOp {
   int32_t srb;       // row stride inside a stage
   int32_t ntiles, nunits, rot;
   int32_t flags;     // OP_WAIT: grid barrier first; OP_NEWX: stage x
+  // first op of an x (OP_NEWX or OP_WAIT) in a program: per CTA the blocks
+  // [lo, hi) of x its units in the ops sharing that x read (lo | hi << 16),
+  // or null (all of x)
+  const int32_t* xrange;
 };
 enum : int32_t { OP_WAIT = 1, OP_NEWX = 2 };
 
@@ -121,7 +125,7 @@ __device__ __forceinline__ void consumer_sync() {
 // ------------------------------------------------------------ work walk
 // Unit k of this CTA in op o: u = ((cta - rot) mod G) + k*G; tile u / KS,
 // K-part u % KS; the part's blocks are split into stages of KC blocks.
-__device__ __forceinline__ int first_unit(const KqOp& o, int cta, int G) {
+__host__ __device__ __forceinline__ int first_unit(const KqOp& o, int cta, int G) {
   int u = cta - (o.rot % G);
   return u < 0 ? u + G : u;
 }
@@ -461,6 +465,10 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
   for (int oi = 0; oi < a.n_ops; ++oi) {
     const KqOp o = nxt;
     if (PROG && oi + 1 < a.n_ops) nxt = load_op<PROG>(a, oi + 1);
+    // the blocks of x this CTA reads until the next x (read before any wait:
+    // the table is written at planning time)
+    int xr = -1;
+    if (PROG && o.xrange && (oi == 0 || (o.flags & (OP_NEWX | OP_WAIT)))) xr = __ldg(o.xrange + cta);
     const bool bf16 = XK0 ? (XK0 == 1) : (o.x_bf16 != 0);  // a program of one x dtype is compiled for it
     if (PROG && oi > 0 && (o.flags & OP_WAIT)) {
       if constexpr (PROG) {
@@ -502,7 +510,8 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
     const XImg xs2[2] = {ximg_at(xbase, a.nb_max), ximg_at(xbase + (a.nimg > 1 ? ximg_stride(a.nb_max) : 0), a.nb_max)};
     if (oi == 0 || (o.flags & (OP_NEWX | OP_WAIT))) {
       consumer_sync();  // every consumer is done with the previous x image
-      stage_x<NTHC>(o.x, bf16 ? 1 : 0, o.K, o.nb, xs2[0], xs2[1], ctid);
+      if (xr < 0) stage_x<NTHC>(o.x, bf16 ? 1 : 0, o.K, o.nb, xs2[0], xs2[1], ctid);
+      else stage_x<NTHC>(o.x, bf16 ? 1 : 0, o.K, o.nb, xs2[0], xs2[1], ctid, xr & 0xFFFF, xr >> 16);
       consumer_sync();
     }
     consume_any<XK0>(o, bf16, xs2, rg, rd, wk, a.err, cta, G);

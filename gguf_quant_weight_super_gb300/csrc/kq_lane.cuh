@@ -282,12 +282,14 @@ __device__ __forceinline__ void put_oct(const float (&v)[8], int o, const XImg& 
 // fp32 x two images, hi and lo.  Thread t takes octs t, t+NTHR, ...; the 32
 // octs of a warp are one block.  All global loads of a pass (up to 6 octs a
 // thread) are issued before any is used.
+// Blocks [b0, b1) of the image (b0 = 0, b1 = nb: all of x).
 template <int NTHR>
-__device__ void stage_x(const void* xp, int x_bf16, int K, int nb, const XImg& xh, const XImg& xl, int tid) {
+__device__ void stage_x(const void* xp, int x_bf16, int K, int nb, const XImg& xh, const XImg& xl, int tid, int b0 = 0,
+                        int b1 = -1) {
   constexpr int MAXO = 6;
-  const int noct = nb * 32;
+  const int noct = (b1 < 0 ? nb : b1) * 32;
   const int lane = tid & 31;
-  for (int base = 0; base < noct; base += MAXO * NTHR) {
+  for (int base = b0 * 32; base < noct; base += MAXO * NTHR) {
     float v[MAXO][8];
 #pragma unroll
     for (int it = 0; it < MAXO; ++it) {
