@@ -329,6 +329,51 @@ def run_single_ffn(args, spec):
     print(json.dumps({"single": args.single, "runs": args.steps, "ok": True}))
 
 
+def run_timeline(args):
+    """Per-stage breakdown of the dense sweep as one chain launch, from the
+    timeline library's per-CTA global-timer stamps (one untimed step after
+    warm-up; the stamps themselves cost a few store instructions per op)."""
+    import torch
+    from gguf_quant_weight_super_gb300 import kq, synth
+    L = kq.use_timeline_library()
+    stages, mats, xs = build_model(torch, synth)
+    chain = make_chain(kq, mats, xs)
+    stream = torch.cuda.Stream()
+    for _ in range(max(3, args.warmup) + 1):
+        chain.run(stream)
+    torch.cuda.synchronize()
+    assert kq.kq_device_error() == 0
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    CT, OPS = 160, 512
+    buf = np.zeros(CT * OPS * 4, dtype=np.uint64)
+    assert L.kq_timeline_read(buf.ctypes.data, buf.nbytes) == 0
+    ts = buf.reshape(CT, OPS, 4).astype(np.int64)[:G] / 1e3  # us
+    starts = [i for i, m in enumerate(mats) if i == 0 or m["stage"] != mats[i - 1]["stage"]] + [len(mats)]
+    rows = []
+    for si in range(len(starts) - 1):
+        i, j = starts[si], starts[si + 1]
+        start, done = ts[:, i, 1], ts[:, j, 3]
+        r = {"stage": si, "ops": "+".join(m["name"].split(".")[-1] for m in mats[i:j]),
+             "bytes": int(sum(m["bytes"] for m in mats[i:j])),
+             "consume_med_us": float(np.median(done - start)),
+             "tail_us": float(done.max() - np.median(done))}
+        if si > 0:
+            r["staging_med_us"] = float(np.median(start - ts[:, i, 0]))
+            r["barrier_us"] = float(ts[:, i, 0].min() - ts[:, i, 3].max())
+            r["stage_us"] = float(done.max() - ts[:, i, 3].max())  # last arrival before to last arrival after
+        rows.append(r)
+    total = float(ts[:, len(mats), 3].max() - ts[:, 0, 1].min())
+    groups = {}
+    for r in rows[1:]:
+        groups.setdefault(r["ops"], []).append(r)
+    out = {"workload": WORKLOAD + ", one chain launch, per-stage means over the layers (us)", "step_us": total,
+           "stages": len(rows)}
+    out["by_stage"] = {k: {f: round(float(np.mean([r[f] for r in v])), 3)
+                           for f in ("bytes", "barrier_us", "staging_med_us", "consume_med_us", "tail_us", "stage_us")}
+                       for k, v in groups.items()}
+    print(json.dumps(out), flush=True)
+
+
 def _timed_graph(torch, fn, stream, steps, warmup):
     g = capture(torch, fn, stream)
     for _ in range(max(3, warmup)):
@@ -659,6 +704,8 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the other configurations in the JSON line")
     ap.add_argument("--single", default=None,
                     help="profiling helper: run one product TYPE:NxK[:M[:f32|bf16]] (e.g. Q4_K:19456x2560), one MoE layer moe_ffn:TYPE:M, or one expansion dequant:TYPE:NxK:fp32|bf16, --steps times")
+    ap.add_argument("--timeline", action="store_true",
+                    help="per-stage breakdown of the dense sweep's chain from per-CTA timer stamps (timeline library)")
     ap.add_argument("--workload", default=None, choices=["q4k_4096", "format_sweep", "verify16", "moe", "dequant"],
                     help="time another configuration instead of the dense sweep (one JSON line each)")
     args = ap.parse_args()
@@ -667,6 +714,9 @@ def main():
         return
     if args.single:
         run_single(args)
+        return
+    if args.timeline:
+        run_timeline(args)
         return
 
     rank = int(os.environ.get("RANK", "0"))

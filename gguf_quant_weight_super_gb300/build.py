@@ -12,6 +12,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 OUT = os.path.join(PKG, "libkq.so")
+TIMELINE_OUT = os.path.join(PKG, "libkq_timeline.so")
 BUILD = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -31,17 +32,23 @@ def _newest_input() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every csrc/*.cu to an object and link libkq.so; returns its path."""
-    if not force and os.path.exists(OUT) and os.path.getmtime(OUT) >= _newest_input():
-        return OUT
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, timeline: bool = False) -> str:
+    """Compile every csrc/*.cu to an object and link libkq.so; returns its path.
+    timeline=True builds libkq_timeline.so instead: the same library with the
+    one-token kernel's per-CTA global-timer stamps (KQ_TIMELINE), for
+    ``bench.py --timeline``."""
+    out = TIMELINE_OUT if timeline else OUT
+    bdir = BUILD + "_timeline" if timeline else BUILD
+    flags = NVCC_FLAGS + (["-DKQ_TIMELINE"] if timeline else [])
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= _newest_input():
+        return out
+    os.makedirs(bdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src).replace(".cu", ".o"))
+        cmd = [cc, *ARCH, *flags, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -53,10 +60,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 8))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = OUT + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     subprocess.check_call([cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs])
-    os.replace(tmp, OUT)
-    return OUT
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

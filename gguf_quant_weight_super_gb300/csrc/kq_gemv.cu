@@ -291,3 +291,12 @@ cudaError_t prog_run(const ProgPlan* plan, void* ws, cudaStream_t stream) {
 }
 
 }  // namespace kq
+
+#ifdef KQ_TIMELINE
+// The timeline library's stamps ([cta][op][4] global-timer values) for the
+// last program launch: copied to host memory dst (bytes at most).
+extern "C" int kq_timeline_read(void* dst, size_t bytes) {
+  const size_t n = bytes < sizeof(kq::g_kq_timeline) ? bytes : sizeof(kq::g_kq_timeline);
+  return static_cast<int>(cudaMemcpyFromSymbol(dst, kq::g_kq_timeline, n));
+}
+#endif

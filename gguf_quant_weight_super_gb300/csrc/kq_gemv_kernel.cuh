@@ -62,6 +62,24 @@ namespace {
 #ifndef KQ_NC
 #define KQ_NC 11
 #endif
+// Built with KQ_TIMELINE (the timeline library only; see build.py): thread 0
+// of every CTA records the global timer at four points of every program op --
+// 0 grid barrier passed, 1 x staged, 3 arriving at the barrier before the op
+// (the previous ops' work done) -- for the first kTlCtas CTAs and kTlOps ops.
+#ifdef KQ_TIMELINE
+constexpr int kTlCtas = 160, kTlOps = 512;
+__device__ unsigned long long g_kq_timeline[kTlCtas * kTlOps * 4];
+__device__ __forceinline__ void tl_mark(int oi, int k) {
+  if (threadIdx.x == 0 && blockIdx.x < kTlCtas && oi < kTlOps) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    g_kq_timeline[(blockIdx.x * kTlOps + oi) * 4 + k] = t;
+  }
+}
+#define KQ_TL(oi, k) tl_mark((oi), (k))
+#else
+#define KQ_TL(oi, k) ((void)0)
+#endif
 constexpr int NC = KQ_NC;              // consumer warps (+1 producer: 12 warps, three warpgroups, 170 registers a thread)
 constexpr int TT = 32;                 // rows per tile (4 per quad)
 constexpr int NTHC = NC * 32;          // consumer threads
@@ -480,10 +498,12 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
       // publish this CTA's outputs so far, then wait for the rest of the grid
       consumer_sync();
       ++barriers;
+      KQ_TL(oi, 3);
       if (ctid == 0) {
         grid_arrive(a.barrier);
         grid_wait(a.barrier, barriers * G, a.err);  // on timeout the error word is set
       }
+      KQ_TL(oi, 0);
       consumer_sync();
       complete = oi;
     }
@@ -514,6 +534,7 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
       else stage_x<NTHC>(o.x, bf16 ? 1 : 0, o.K, o.nb, xs2[0], xs2[1], ctid, xr & 0xFFFF, xr >> 16);
       consumer_sync();
     }
+    KQ_TL(oi, 1);
     consume_any<XK0>(o, bf16, xs2, rg, rd, wk, a.err, cta, G);
   }
   if constexpr (PROG) {  // sums complete since the last barrier
@@ -521,6 +542,10 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
       const KqOp f = load_op<PROG>(a, fixed);
       if (f.KS > 1) fixup_op(f, cta, G, ctid);
     }
+  }
+  if constexpr (PROG) {
+    consumer_sync();
+    KQ_TL(a.n_ops, 3);  // all of this CTA's ops done
   }
   if (PROG && a.barrier) {
     // final barrier (only when split-K sums of the last stage remain), then

@@ -91,6 +91,21 @@ class KQError(RuntimeError):
 _lib = None
 
 
+def use_timeline_library() -> ctypes.CDLL:
+    """Build and load libkq_timeline.so (the library with the one-token
+    kernel's per-CTA timer stamps) in place of libkq.so; call before any other
+    use of the library in the process."""
+    global LIB_PATH
+    if _lib is not None:
+        raise RuntimeError("the library is already loaded")
+    from . import build
+    LIB_PATH = build.build(timeline=True)
+    L = lib()
+    L.kq_timeline_read.restype = ctypes.c_int
+    L.kq_timeline_read.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    return L
+
+
 def lib() -> ctypes.CDLL:
     """Load libkq.so (built in-tree by ``gguf_quant_weight_super_gb300.build``)."""
     global _lib
