@@ -206,14 +206,19 @@ struct Walk {
 
 // Consumers: every unit of op o for this CTA.  Quad q of every warp owns the
 // tile rows q, q+8, ... (R of them; a tile is 8R rows).  A stage's blocks are
-// dealt to the warps in pairs (continuing across stages): lanes c of every
+// dealt to the warps (continuing across stages) in pairs -- lanes c of every
 // quad take block 2g + (c >> 1) of pair g, half c & 1 of it (two 64-weight
 // chunks, one 128-value run), for the R rows of the quad, and combine once per
-// row and half.  NI x images: with
+// row and half -- or, with BLK, one by one: lane c takes chunk c of the block
+// and combines once per row and chunk.  NI x images: with
 // SUM they are the hi and lo images of one fp32 x (one output), else NI
 // tokens' bf16 x (y is [NI][N]; each token's rows take exactly the one-token
 // arithmetic).
-template <int QT, int R, int NI, bool SUM>
+// BLK: the items dealt to the warps are single blocks (lane c = chunk c, one
+// combine per chunk; programs: twice the items per stage, so a stage's slot
+// is released sooner -- dense sweep chain 1.42 -> 1.36 ms) instead of pairs
+// (single products: fewer combines -- the long Q4_K product 3.38 -> 3.77 TB/s).
+template <int QT, int R, int NI, bool SUM, bool BLK = false>
 __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, const Red& rd, Walk& wk, int* err,
                            int cta, int G) {
   constexpr int BB = Fmt<QT>::BYTES;
@@ -232,7 +237,7 @@ __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, 
       for (int i = 0; i < R; ++i) acc[t][i] = 0.0f;
     for (int b0 = kb0; b0 < kb1; b0 += o.KC) {
       const int n = min(o.KC, kb1 - b0);
-      const int ng = (n + 1) >> 1;  // pairs of blocks
+      const int ng = BLK ? n : (n + 1) >> 1;  // items: blocks, or pairs of blocks
       const int slot = wk.slot;
       if (!wk.failed) {
         const bool ok = mbar_wait(&rg.full[slot], wk.phase, err);
@@ -253,11 +258,22 @@ __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, 
           // (one offset for a stage copied as one block)
           const uint32_t off =
               (seg0 + (o.contig ? 0u : static_cast<uint32_t>(r) * static_cast<uint32_t>(o.row_bytes))) & 15u;
-          rp[i] = sp + r * o.srb + off + (2 * gi + (c >> 1)) * BB;
+          rp[i] = sp + r * o.srb + off + (BLK ? gi : 2 * gi + (c >> 1)) * BB;
         }
+        const ScaleLane sl = scale_lane(c);
         for (; gi < ng; gi += NC) {
-          const int bl = 2 * gi + (c >> 1);  // this lane's block within the stage
-          if (bl < n) {
+          const int bl = BLK ? gi : 2 * gi + (c >> 1);  // this lane's block within the stage
+          if constexpr (BLK) {
+            const int b = b0 + bl;
+            if constexpr (SUM) {
+#pragma unroll 1
+              for (int t = 0; t < NI; ++t)
+                block_rows<QT, R>(t ? xs[NI - 1] : xs[0], b, rp, c, sl, t ? kLimBf16 : kLimHi, acc[0]);
+            } else {
+#pragma unroll
+              for (int t = 0; t < NI; ++t) block_rows<QT, R>(xs[t], b, rp, c, sl, kLimBf16, acc[t]);
+            }
+          } else if (bl < n) {
             const int b = b0 + bl;
             // the hi image of fp32 x takes the tighter fp32 combine check
             // (kLimHi), bf16 images and the lo image (2^-9 of the value) kLimBf16
@@ -271,7 +287,7 @@ __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, 
             }
           }
 #pragma unroll
-          for (int i = 0; i < R; ++i) rp[i] += 2 * NC * BB;
+          for (int i = 0; i < R; ++i) rp[i] += (BLK ? 1 : 2) * NC * BB;
         }
       }
       wk.cb = (wk.cb + ng) % NC;
@@ -345,9 +361,9 @@ template <int QT, int XK0>
 __device__ __forceinline__ void consume_bf16(const KqOp& o, const XImg (&x1)[1], const Ring& rg, const Red& rd,
                                              Walk& wk, int* err, int cta, int G) {
   if constexpr (QT == T_Q6_K) {  // Q6_K ops whose 32-row stage would not fit the chain's slots take 16 rows
-    if (o.R == 2) { consume_op<QT, 2, 1, false>(o, x1, rg, rd, wk, err, cta, G); return; }
+    if (o.R == 2) { consume_op<QT, 2, 1, false, true>(o, x1, rg, rd, wk, err, cta, G); return; }
   }
-  consume_op<QT, 4, 1, false>(o, x1, rg, rd, wk, err, cta, G);
+  consume_op<QT, 4, 1, false, true>(o, x1, rg, rd, wk, err, cta, G);
 }
 template <int XK0>
 __device__ __forceinline__ void consume_any(const KqOp& o, bool bf16, const XImg (&xs)[2], const Ring& rg,
@@ -358,9 +374,9 @@ __device__ __forceinline__ void consume_any(const KqOp& o, bool bf16, const XImg
     else if (o.type == T_Q5_K) consume_bf16<T_Q5_K, XK0>(o, x1, rg, rd, wk, err, cta, G);
     else consume_bf16<T_Q6_K, XK0>(o, x1, rg, rd, wk, err, cta, G);
   } else {
-    if (o.type == T_Q4_K) consume_op<T_Q4_K, 4, 2, true>(o, xs, rg, rd, wk, err, cta, G);
-    else if (o.type == T_Q5_K) consume_op<T_Q5_K, 4, 2, true>(o, xs, rg, rd, wk, err, cta, G);
-    else consume_op<T_Q6_K, 4, 2, true>(o, xs, rg, rd, wk, err, cta, G);
+    if (o.type == T_Q4_K) consume_op<T_Q4_K, 4, 2, true, true>(o, xs, rg, rd, wk, err, cta, G);
+    else if (o.type == T_Q5_K) consume_op<T_Q5_K, 4, 2, true, true>(o, xs, rg, rd, wk, err, cta, G);
+    else consume_op<T_Q6_K, 4, 2, true, true>(o, xs, rg, rd, wk, err, cta, G);
   }
 }
 
