@@ -235,6 +235,8 @@ __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, 
     for (int t = 0; t < MT; ++t)
 #pragma unroll
       for (int i = 0; i < R; ++i) acc[t][i] = 0.0f;
+    int items = 0;      // items of the unit (all warps)
+    bool mine = false;  // this warp has an item in the unit
     for (int b0 = kb0; b0 < kb1; b0 += o.KC) {
       const int n = min(o.KC, kb1 - b0);
       const int ng = BLK ? n : (n + 1) >> 1;  // items: blocks, or pairs of blocks
@@ -245,6 +247,8 @@ __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, 
       }
       int gi = warp - wk.cb;
       if (gi < 0) gi += NC;
+      mine = mine || gi < ng;
+      items += ng;
       if (!wk.failed && gi < ng) {
         // the quad's rows q, q+8, q+16, q+24 (rows past N are computed on
         // stale shared memory and never written)
@@ -295,6 +299,12 @@ __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, 
       if (lane == 0) mbar_arrive(&rg.empty[slot]);
       if (++wk.slot == rg.S) { wk.slot = 0; wk.phase ^= 1u; }
     }
+    // A unit's buffer is used again RS = S + 1 units later: a warp reaches
+    // that unit only after every warp has passed a later stage of the ring,
+    // which the unit's last warp does only after adding the unit up.
+    const int rs = wk.rs;
+    if (++wk.rs == rd.RS) wk.rs = 0;
+    if (!mine) continue;  // no item in the unit: its buffer row stays zero
     // this warp's partial row sums: over the quad's lanes, then to shared memory
 #pragma unroll
     for (int t = 0; t < MT; ++t)
@@ -303,8 +313,6 @@ __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, 
         acc[t][i] = __fadd_rn(acc[t][i], __shfl_xor_sync(0xFFFFFFFFu, acc[t][i], 1));
         acc[t][i] = __fadd_rn(acc[t][i], __shfl_xor_sync(0xFFFFFFFFu, acc[t][i], 2));
       }
-    const int rs = wk.rs;
-    if (++wk.rs == rd.RS) wk.rs = 0;
     float* rb = rd.buf + static_cast<size_t>(rs) * NC * TT * MT;  // [MT][NC][TT]
     if (c == 0) {
 #pragma unroll
@@ -316,11 +324,12 @@ __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, 
     int last = 0;
     if (lane == 0) {
       __threadfence_block();
-      last = (atomicAdd(&rd.cnt[rs], 1) == NC - 1) ? 1 : 0;
+      last = (atomicAdd(&rd.cnt[rs], 1) == min(items, NC) - 1) ? 1 : 0;  // the warps with an item
     }
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
     if (!last) continue;
-    // last warp of the unit: add the warps' partials in warp order
+    // last warp of the unit: add the NC partials in warp order (zero where a
+    // warp had no item), then clear them
     __threadfence_block();
     float v[MT];
 #pragma unroll
@@ -328,6 +337,8 @@ __device__ void consume_op(const KqOp& o, const XImg (&xs)[NI], const Ring& rg, 
       v[t] = rb[t * NC * TT + lane];
 #pragma unroll
       for (int w = 1; w < NC; ++w) v[t] = __fadd_rn(v[t], rb[(t * NC + w) * TT + lane]);
+#pragma unroll
+      for (int w = 0; w < NC; ++w) rb[(t * NC + w) * TT + lane] = 0.0f;
     }
     __syncwarp();
     if (lane == 0) rd.cnt[rs] = 0;
@@ -453,6 +464,7 @@ __global__ void __launch_bounds__(NTH, 1) prog_kernel(const __grid_constant__ Pr
     for (int s = 0; s < a.S; ++s) { mbar_init(&rg.full[s], 1); mbar_init(&rg.empty[s], NC); }
     for (int s = 0; s <= a.S; ++s) rd.cnt[s] = 0;
   }
+  for (size_t i = threadIdx.x; i < red_bytes(a.S, MT0) / 4; i += NTH) rd.buf[i] = 0.0f;
   fence_mbar_init();
   __syncthreads();
 
