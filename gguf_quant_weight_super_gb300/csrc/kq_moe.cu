@@ -92,9 +92,17 @@ __host__ __device__ inline size_t moe_ximg_offset() { return (sizeof(MoeSmem) + 
 // rp, rp + rstride, ...; nph quads per row, the quad of phase ph taking blocks
 // ph, ph + nph, ...): each block's x slice is loaded once for all RQ rows.
 // NI x images (fp32 x: hi and lo) add into the same sums.
+// (Out of line, one copy per rows-per-quad: the kernel calls it for up to three
+// tile shapes and two matrices, and inlined copies overflowed the instruction
+// cache.)
+template <int NI>
+struct XImgs {
+  XImg v[NI];
+};
 template <int QT, int NI, int RQ>
-__device__ __forceinline__ void pair_rows(uint32_t rp, uint32_t rstride, int nb, const XImg (&xs)[NI], int ph,
-                                          int nph, int c, const ScaleLane& sl, float (&acc)[4]) {
+__device__ __noinline__ float4 pair_rows_ol(uint32_t rp, uint32_t rstride, int nb, const XImgs<NI> xs_, int ph,
+                                            int nph, int c, const ScaleLane sl) {
+  const XImg (&xs)[NI] = xs_.v;
   constexpr int BB = Fmt<QT>::BYTES;
   float a[RQ];
 #pragma unroll
@@ -112,8 +120,19 @@ __device__ __forceinline__ void pair_rows(uint32_t rp, uint32_t rstride, int nb,
     v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
     v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
     for (int o = 4; o < 4 * nph; o <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    acc[i] = v;
+    a[i] = v;
   }
+  return make_float4(a[0], RQ > 1 ? a[RQ > 1 ? 1 : 0] : 0.0f, RQ > 2 ? a[RQ > 2 ? 2 : 0] : 0.0f,
+                     RQ > 3 ? a[RQ > 3 ? 3 : 0] : 0.0f);
+}
+template <int QT, int NI, int RQ>
+__device__ __forceinline__ void pair_rows(uint32_t rp, uint32_t rstride, int nb, const XImg (&xs)[NI], int ph,
+                                          int nph, int c, const ScaleLane& sl, float (&acc)[4]) {
+  XImgs<NI> xv;
+#pragma unroll
+  for (int t = 0; t < NI; ++t) xv.v[t] = xs[t];
+  const float4 r = pair_rows_ol<QT, NI, RQ>(rp, rstride, nb, xv, ph, nph, c, sl);
+  acc[0] = r.x; acc[1] = r.y; acc[2] = r.z; acc[3] = r.w;
 }
 
 // The activation of the gate|up mode, in fp32 with CUDA's expf / tanhf.
@@ -125,7 +144,7 @@ __device__ __forceinline__ float ffn_act(int act, float g) {
 }
 
 template <int QT, int XK>
-__global__ void __launch_bounds__(MTH) moe_kernel(const __grid_constant__ MoeArgs a) {
+__global__ void __launch_bounds__(MTH, 2) moe_kernel(const __grid_constant__ MoeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   MoeSmem& sm = *reinterpret_cast<MoeSmem*>(smem + 16);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
