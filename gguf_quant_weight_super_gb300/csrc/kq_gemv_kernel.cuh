@@ -7,22 +7,21 @@
 // section "Keeping the CPU and GPU working together": the device should not
 // idle between the operations of a decode step.
 //
-// Arithmetic (exact integer products, one rounding per lane and block; see
-// kq_lane.cuh):
-//  * x is staged once per product into shared memory as an exact image: for
-//    every run of 128 values a power-of-two scale s = 2^(e-22), e the binary
-//    exponent of the run's largest |x|; values on that grid (every bf16 value
-//    within 2^15 of the run maximum) as 24-bit integers m = x/s in three byte
-//    limbs, the others listed with their block by index and bf16 value.  fp32
-//    x is staged as two such images, hi = bf16(x) and lo = bf16(x - hi);
-//  * a lane owns 64 weights of a block (Q4_K/Q5_K: sub-blocks 2c, 2c+1;
-//    Q6_K: four 16-runs of one 128-half); codes times limbs are summed
-//    exactly by dp4a and the lane's block contribution
+// Arithmetic (exact integer products; see kq_lane.cuh):
+//  * x is staged into shared memory as an exact image: for every block of 256
+//    values a power-of-two scale s = 2^(e-22), e the binary exponent of the
+//    block's largest |x|; values on that grid (every bf16 value within 2^15 of
+//    the block maximum) as 24-bit integers m = x/s in three byte limbs, the
+//    others listed beside the block (index and bf16 value; past 32 of them the
+//    block keeps all 256 values as bf16).  fp32 x is staged as two such
+//    images, hi = bf16(x) and lo = bf16(x - hi);
+//  * a lane owns a 64-weight chunk or a 128-weight half of a block; codes
+//    times limbs are summed exactly by dp4a and the lane's contribution
 //        Q4_K/Q5_K:  y += s * (d * sum_p sc_p*T_p  -  dmin * sum_p m_p*X_p)
 //        Q6_K:       y += s * d * sum_p sc_p*(T_p - 32*X_p)
-//    (T_p = sum q*m, X_p = sum m over part p) is formed from exact integers and
-//    rounded once; a listed value adds fl(w*x) with w the exactly rounded fp32
-//    weight.
+//    (T_p = sum q*m, X_p = sum m over part p) is formed from exact integers
+//    and rounded to fp32 within a proven bound (combine45_checked); listed and
+//    kept values add fl(w*x) with w the exactly rounded fp32 weight.
 
 // Execution (GB300: 152 SMs, 227 KB shared memory per CTA):
 //  * one CTA per SM: a producer warp and NC consumer warps;
