@@ -67,9 +67,12 @@ def job_gbs(bytes_per_replica, world, ms):
     return bytes_per_replica * world / (ms * 1e-3) / 1e9
 
 
-def build_model(torch, synth, seed=0):
-    """Weights and per-stage inputs/outputs for one token of the sweep."""
+def build_model(torch, synth, seed=0, n_stages=None):
+    """Weights and per-stage inputs/outputs for one token of the sweep (its
+    first n_stages stages only, when given)."""
     stages = synth.dense_layer_sweep()
+    if n_stages is not None:
+        stages = stages[:n_stages]
     dev = torch.device("cuda")
     mats, xs = [], []
     # every stage's x is a view of one device buffer (xs[0]._base), so a
@@ -270,6 +273,8 @@ def run_single(args):
         return run_single_ffn(args, spec)
     if spec[0] == "dequant":  # dequant:<type>:<N>x<K>:<fp32|bf16>: expansion of a whole matrix
         return run_single_dequant(args, spec)
+    if spec[0] == "chain":  # chain:<layers>: the dense sweep's first layers as one chain launch
+        return run_single_chain(args, int(spec[1]) if len(spec) > 1 else 1)
     qt = {"Q4_K": synth.Q4_K, "Q5_K": synth.Q5_K, "Q6_K": synth.Q6_K, "IA4": synth.IA4}[spec[0]]
     N, K = (int(v) for v in spec[1].split("x"))
     M = int(spec[2]) if len(spec) > 2 else 1
@@ -284,6 +289,21 @@ def run_single(args):
     torch.cuda.synchronize()
     assert kq.kq_device_error() == 0
     print(json.dumps({"single": args.single, "runs": args.steps, "ok": True}))
+
+
+def run_single_chain(args, layers):
+    """The first `layers` layers of the dense sweep (4 dependent stages each)
+    as one chain launch, `--steps` times (for profiler captures)."""
+    import torch
+    from gguf_quant_weight_super_gb300 import kq, synth
+    stages, keep, xs = build_model(torch, synth, n_stages=4 * layers)
+    chain = make_chain(kq, keep, xs)
+    for _ in range(args.steps):
+        chain.run()
+    torch.cuda.synchronize()
+    assert kq.kq_device_error() == 0
+    print(json.dumps({"single": args.single, "runs": args.steps, "ok": True,
+                      "weight_bytes": int(sum(m["bytes"] for m in keep))}))
 
 
 def run_single_dequant(args, spec):
@@ -705,7 +725,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other configurations in the JSON line")
     ap.add_argument("--single", default=None,
-                    help="profiling helper: run one product TYPE:NxK[:M[:f32|bf16]] (e.g. Q4_K:19456x2560), one MoE layer moe_ffn:TYPE:M, or one expansion dequant:TYPE:NxK:fp32|bf16, --steps times")
+                    help="profiling helper: run one product TYPE:NxK[:M[:f32|bf16]] (e.g. Q4_K:19456x2560), one MoE layer moe_ffn:TYPE:M, one expansion dequant:TYPE:NxK:fp32|bf16, or the dense sweep's first layers as a chain chain:LAYERS, --steps times")
     ap.add_argument("--timeline", action="store_true",
                     help="per-stage breakdown of the dense sweep's chain from per-CTA timer stamps (timeline library)")
     ap.add_argument("--workload", default=None, choices=["q4k_4096", "format_sweep", "verify16", "moe", "dequant"],
